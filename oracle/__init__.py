@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the causal grouped-query attention forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import this package.  The
+product path (``transformer_causal_gqa_gb300``) never imports it and has no
+CPU fallback.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64); this module only
+compiles it with gcc (once, into ``oracle/_build/``) and marshals numpy arrays
+through ctypes.  What it computes follows the page
+"Realization/Nvidia/SM86/StreamingAttentionSM86.alpha", header comment:
+softmax(Q K^T scale) V per query head in base-2 units, t = S c, weights
+2^(t - m), output O / l and log-sum-exp m + log2 l.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+HEAD_DIM = 64
+
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile attn_oracle.c into a shared library (OpenMP if gcc supports it)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    fresh = os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src)
+    if fresh and not force:
+        return out
+    tmp = out + f".{os.getpid()}.tmp"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, out)
+    return out
+
+
+def open_library(path: str):
+    """ctypes handle on a compiled oracle library, with its signatures declared."""
+    lib = ctypes.CDLL(path)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_float,
+                                    f64p, f64p, ctypes.c_int]
+    lib.oracle_attn_fwd.restype = ctypes.c_int
+    lib.oracle_attn_fwd_rows.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_float,
+                                         i64p, i64p, i64, f64p, f64p, ctypes.c_int]
+    lib.oracle_attn_fwd_rows.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = open_library(build())
+    return _lib
+
+
+def _bits(a: np.ndarray, shape: tuple) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.float16:
+        raise TypeError("oracle inputs are binary16 arrays")
+    if a.shape != shape:
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a.view(np.uint16)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def half_to_double(bits: int) -> float:
+    """Exact value of one binary16 bit pattern, decoded by the oracle's own routine."""
+    return float(_load().oracle_half_to_double(int(bits) & 0xFFFF))
+
+
+def max_threads() -> int:
+    """Threads the oracle uses when ``threads`` is not given."""
+    return int(_load().oracle_max_threads())
+
+
+def attn_fwd(q: np.ndarray, k: np.ndarray, vT: np.ndarray, T: int, heads: int,
+             kv_heads: int, c: float, threads: int = 0, lib=None):
+    """Every row.  Returns (O float64 [T][heads*64], LSE float64 [heads][T])."""
+    lib = lib or _load()
+    qb = _bits(q, (heads, T, HEAD_DIM))
+    kb = _bits(k, (kv_heads, T, HEAD_DIM))
+    vb = _bits(vT, (kv_heads, HEAD_DIM, T))
+    o = np.empty((T, heads * HEAD_DIM), dtype=np.float64)
+    lse = np.empty((heads, T), dtype=np.float64)
+    rc = lib.oracle_attn_fwd(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                             _ptr(vb, ctypes.c_uint16), T, heads, kv_heads,
+                             ctypes.c_float(c), _ptr(o, ctypes.c_double),
+                             _ptr(lse, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return o, lse
+
+
+def attn_fwd_rows(q: np.ndarray, k: np.ndarray, vT: np.ndarray, T: int, heads: int,
+                  kv_heads: int, c: float, heads_idx, rows_idx, threads: int = 0,
+                  lib=None):
+    """Selected (head, row) pairs.  Returns (O float64 [n][64], LSE float64 [n])."""
+    lib = lib or _load()
+    qb = _bits(q, (heads, T, HEAD_DIM))
+    kb = _bits(k, (kv_heads, T, HEAD_DIM))
+    vb = _bits(vT, (kv_heads, HEAD_DIM, T))
+    hi = np.ascontiguousarray(heads_idx, dtype=np.int64)
+    ri = np.ascontiguousarray(rows_idx, dtype=np.int64)
+    if hi.shape != ri.shape or hi.ndim != 1:
+        raise ValueError("heads_idx and rows_idx must be 1-D and equal length")
+    n = hi.shape[0]
+    o = np.empty((n, HEAD_DIM), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    rc = lib.oracle_attn_fwd_rows(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                  _ptr(vb, ctypes.c_uint16), T, heads, kv_heads,
+                                  ctypes.c_float(c), _ptr(hi, ctypes.c_int64),
+                                  _ptr(ri, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
+                                  _ptr(lse, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape or an index")
+    return o, lse
