@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Causal GQA attention forward benchmark on GB300.
+
+Metric: causal attention forward TFLOP/s, counting 4 * T^2 * 64 * heads / 2
+FLOPs per pass, on the headline workload (T = 8192, 32 query heads over 8 K/V
+heads, head width 64, binary16 inputs from the seeded generator), and its
+fraction of the GB300's dense fp16 tensor peak.
+
+One step = one forward pass (one kernel launch) over the whole workload.
+Inputs are resident in HBM; the 129 MB L2 is flushed (a 512 MiB write)
+between timed steps because the workload's inputs (85 MB) would otherwise stay
+in it.  Each launch is timed with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+For N > 1 (torchrun), every rank runs its own independent problem of the same
+shape (weak scaling, no collective on the data path); the barrier and the
+max-over-ranks timing use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import dataclasses
+import hashlib
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s and % of GB300 dense fp16 tensor peak, T=8192"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FLUSH_BYTES = 512 << 20
+KERNEL_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_fwd.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_t8192_h32_kv8.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "T": w.T, "heads": w.heads, "kv_heads": w.kv_heads,
+            "head_dim": 64, "group": w.group, "causal_flops_per_step": w.causal_flops,
+            "inputs": "seeded synthetic binary16 (Philox), c = fl32(0.125/ln 2)",
+            "l2": l2_note}
+
+
+def sampled_flops(rows):
+    """FLOPs the metric credits a sample of query rows: 4 * 64 per causal (row, key) pair."""
+    return float(256.0 * (np.asarray(rows, dtype=np.float64) + 1.0).sum())
+
+
+def oracle_sample(w, inputs, n_rows, seed):
+    import oracle
+    q, k, vT = inputs
+    rng = np.random.default_rng(seed)
+    hs = rng.integers(0, w.heads, n_rows)
+    rs = rng.integers(0, w.T, n_rows)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q, k, vT, w.T, w.heads, w.kv_heads, synthetic.scale_c(), hs, rs)
+    return time.perf_counter() - t0, sampled_flops(rs)
+
+
+def calibrate_rows(w, inputs, target_s):
+    """Rows of the workload the oracle covers in about target_s seconds."""
+    n = 64
+    while True:
+        dt, _ = oracle_sample(w, inputs, n, seed=1)
+        if dt > 0.5 or n >= 1 << 22:
+            break
+        n *= 4
+    return max(8, int(n * target_s / max(dt, 1e-6)))
+
+
+def cpu_baseline(w, inputs, target_s=15.0):
+    import oracle
+    n = calibrate_rows(w, inputs, target_s)
+    dt, fl = oracle_sample(w, inputs, n, seed=2)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{n} query rows of {w.name} drawn uniformly over heads and rows "
+                      f"(fp64 two-pass oracle, {dt:.1f} s); FLOPs credited 256 per causal "
+                      f"(row, key) pair as in the metric"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for rec in csv.reader(f):
+                if len(rec) >= 9:
+                    rows.append([x.strip() for x in rec])
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_uuid():
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- roofline
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst; fp16 dense rate = bf16)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16; fp16 dense rate = bf16)"
+
+
+def kernel_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and m_h):
+        return None
+    cur = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if cur == m_h.group(1) else None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gb300(args):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        tcg_build.build()
+    if world > 1:
+        dist.barrier()
+    tcg.load_library()
+
+    base = synthetic.WORKLOADS[args.workload]
+    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)   # an independent problem per rank
+    inputs = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
+    o = torch.empty((w.T, w.heads * 64), dtype=torch.float16, device=dev)
+    lse = torch.empty((w.heads, w.T), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tcg.attn_fwd(q, k, vT, o, lse, w.T, w.heads, w.kv_heads, c, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    if tcg.last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("device status after warm-up is not OK")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid())
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()               # evict the previous step's inputs from L2
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if tcg.last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("device status after the timed steps is not OK")
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_s = sum(per_launch_ms) / 1e3
+
+    # end to end through the host-buffer entry point: H2D inputs, kernel, D2H outputs
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in inputs)
+    oh = torch.empty((w.T, w.heads * 64), dtype=torch.float16).pin_memory()
+    lh = torch.empty((w.heads, w.T), dtype=torch.float32).pin_memory()
+    ws = torch.empty(tcg.attn_fwd_workspace_bytes(w.T, w.heads, w.kv_heads),
+                     dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        tcg.attn_fwd_host(qh, kh, vh, oh, lh, w.T, w.heads, w.kv_heads, c, ws, stream)
+
+    for _ in range(3):
+        e2e_step()
+    E = max(1, args.e2e_steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+        stream.synchronize()        # the result is on the host before the next step
+    e2e_s = time.perf_counter() - e0
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+
+    if rank == 0:
+        flops = w.causal_flops
+        value = world * K * flops / dev_s / 1e12
+        avg_launch_s = statistics.fmean(per_launch_ms) / 1e3
+        achieved = flops / avg_launch_s / 1e12
+        peak, peak_note = measured_peak()
+        traffic = kernel_traffic()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": dev_s / K * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": dict(workload_config(w, "flushed between timed steps (512 MiB write); "
+                                              "each launch timed by CUDA events"),
+                           parallelism=f"independent problem per GPU x{world}"),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_note,
+                         "kernel": "attn_fwd_kernel",
+                         "launch_ms": {"mean": avg_launch_s * 1e3,
+                                       "median": statistics.median(per_launch_ms),
+                                       "min": min(per_launch_ms)}},
+            "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "attn_fwd_host: pinned host buffers, copies + kernel on one stream, "
+                            "synchronised each step"},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(base, inputs)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    import oracle
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    inputs = synthetic.make_inputs(w)
+    K, W = max(1, args.steps), max(3, args.warmup)
+    budget_s = 120.0
+    rows = calibrate_rows(w, inputs, budget_s / (K + W))
+    for i in range(W):
+        oracle_sample(w, inputs, rows, seed=100 + i)
+    tot_s = tot_fl = 0.0
+    for i in range(K):
+        dt, fl = oracle_sample(w, inputs, rows, seed=1000 + i)
+        tot_s += dt
+        tot_fl += fl
+    value = tot_fl / tot_s / 1e12
+    sample = (f"each step: {rows} query rows of {w.name} drawn uniformly over heads and rows; "
+              f"FLOPs credited 256 per causal (row, key) pair as in the metric")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": tot_s / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(workload_config(w, "not applicable (host CPU)"),
+                       parallelism="host cores of rank 0"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,117 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention
+ * forward pass, computed as a streaming normalised sum.
+ *
+ * The operation is the one stated in the header comment of the page
+ * "Realization/Nvidia/SM86/StreamingAttentionSM86.alpha": for every query
+ * head h (reading compact K/V head g = floor(h / (heads / kv_heads)), the
+ * page's grid mapping "head = kvHead * groups + z") and every query row i,
+ *
+ *   t_ij = c * sum_e Q[h][i][e] K[g][j][e]      for keys j <= i (causal, diagonal kept)
+ *   O[i][h*64 + e] = sum_j 2^(t_ij - m_i) V^T[g][e][j] / l_i
+ *   LSE[h][i]      = m_i + log2 l_i             (base 2)
+ *
+ * with m_i = max_j t_ij and l_i = sum_j 2^(t_ij - m_i).  c is the binary32
+ * nearest scale / ln 2 (for head width 64, scale = 1/8).  As on that page,
+ * the weights 2^(t - m) are rounded to binary16 only for their product with
+ * V; the running maximum, the running sum and the weighted sum stay binary32.
+ *
+ * Layouts (all row-major, the page's argument block "pointers to Q, K, V^T,
+ * O and L, then c"):
+ *   q    binary16 [heads][T][64]
+ *   k    binary16 [kv_heads][T][64]
+ *   vT   binary16 [kv_heads][64][T]    (V transposed per K/V head)
+ *   o    binary16 [T][heads*64]        (token-major, heads merged)  -- output
+ *   lse  binary32 [heads][T]           (base-2 log-sum-exp)          -- output
+ *
+ * Ownership: the caller owns every buffer.  The library keeps, per device,
+ * one 4-byte status word it allocates on first use and never frees; it
+ * allocates nothing per call.
+ *
+ * Errors: every entry point returns an attn_status.  Argument errors are
+ * detected on the host before anything is launched.  The launches are
+ * asynchronous and ordered on `stream` like a kernel launch.
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (NULL = the legacy default stream). */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_EINVAL = -1,   /* a size or the scale is outside what the operation admits */
+    ATTN_EALIGN = -2,   /* a pointer is not 16-byte aligned */
+    ATTN_EOVERLAP = -3, /* an output overlaps an input or the other output */
+    ATTN_ELAUNCH = -4,  /* the CUDA runtime refused a copy, the set-up or the launch */
+    ATTN_EDEVICE = -5,  /* no current CUDA device, or it is not an sm_103 (GB300) part */
+    ATTN_ETIMEOUT = -6  /* a kernel wait gave up (reported by attn_last_device_status) */
+} attn_status;
+
+/* Largest number of query heads admitted (the page's limit of 65535). */
+#define ATTN_MAX_HEADS 65535
+/* Head width: the only one the page defines. */
+#define ATTN_HEAD_DIM 64
+
+/*
+ * attn_fwd -- the forward pass on device buffers.
+ *
+ * q, k, vT, o, lse: device pointers, 16-byte aligned, layouts above.
+ * T: sequence length; T > 0 and T % 64 == 0.
+ * heads, kv_heads: heads > 0, kv_heads > 0, heads % kv_heads == 0,
+ *   heads <= 65535, and heads * 64 * T * 4 <= 2^32 - 1 (the page's admission
+ *   predicate for the forward program).
+ * c: finite and > 0.
+ * stream: the stream to run on.
+ *
+ * Returns ATTN_OK once the kernel is queued; ATTN_EINVAL / ATTN_EALIGN /
+ * ATTN_EOVERLAP before anything is queued if an argument is bad;
+ * ATTN_EDEVICE without a suitable device; ATTN_ELAUNCH if the runtime
+ * rejects the launch.  Every element of o and lse is written.
+ */
+int attn_fwd(const void *q, const void *k, const void *vT, void *o, float *lse,
+             int T, int heads, int kv_heads, float c, cudaStream_t stream);
+
+/*
+ * attn_fwd_workspace_bytes -- device bytes attn_fwd_host needs for the given
+ * shape (Q, K, V^T, O and LSE packed at 256-byte boundaries), or 0 if the
+ * shape is not admitted.
+ */
+size_t attn_fwd_workspace_bytes(int T, int heads, int kv_heads);
+
+/*
+ * attn_fwd_host -- the forward pass on HOST buffers (same layouts as
+ * attn_fwd).  Queues on `stream`: copies of q, k, vT into `workspace` (a
+ * device buffer of at least attn_fwd_workspace_bytes bytes, 256-byte aligned,
+ * owned by the caller), the kernel, and copies of O and LSE back into o and
+ * lse.  Host buffers should be page-locked for the copies to be asynchronous;
+ * the caller synchronises `stream` before reading o and lse.
+ * Errors as attn_fwd; ATTN_EINVAL also if workspace_bytes is too small.
+ */
+int attn_fwd_host(const void *q, const void *k, const void *vT, void *o, float *lse,
+                  int T, int heads, int kv_heads, float c,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_last_device_status -- synchronises `stream`, then returns and clears
+ * the current device's status word: ATTN_OK, or ATTN_ETIMEOUT if a wait
+ * inside a kernel gave up since the last call (the kernel then wrote no
+ * trustworthy output and exited cleanly).  ATTN_ELAUNCH if the synchronisation
+ * itself reports a CUDA error.
+ */
+int attn_last_device_status(cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

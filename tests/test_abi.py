@@ -1,0 +1,105 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every
+symbol include/attn_fwd.h declares, and rejects bad arguments before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_causal_gqa_gb300 as tcg
+from transformer_causal_gqa_gb300 import build as tcg_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tcg_build.build()
+    return tcg.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(attn_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names == set(tcg.EXPORTED)
+    for n in names:
+        assert getattr(lib, n) is not None
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        assert tcg.status_string(code) != "unknown status"
+    assert tcg.status_string(7) == "unknown status"
+
+
+def call(lib, q=0x1000, k=0x100000, v=0x200000, o=0x300000, l=0x400000, T=128, H=4, G=2, c=0.18):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(vp(q), vp(k), vp(v), vp(o), vp(l), T, H, G, c, None)
+
+
+@pytest.mark.parametrize("T,H,G,c", [
+    (0, 4, 2, 0.18), (100, 4, 2, 0.18), (-64, 4, 2, 0.18),   # T > 0, T % 64 == 0
+    (128, 0, 1, 0.18), (128, 4, 0, 0.18), (128, 4, 3, 0.18),  # heads % kv_heads == 0
+    (128, 65536, 1, 0.18),                                    # heads <= 65535
+    (2 ** 24, 1, 1, 0.18),                                     # heads*64*T*4 <= 2^32-1
+    (128, 4, 2, 0.0), (128, 4, 2, -1.0), (128, 4, 2, float("inf")), (128, 4, 2, float("nan")),
+])
+def test_rejects_inadmissible_shapes(lib, T, H, G, c):
+    assert call(lib, T=T, H=H, G=G, c=c) == tcg.ATTN_EINVAL
+
+
+def test_admission_boundary(lib):
+    # heads*64*T*4 == 2^32 exactly is one past the limit; 2^32 - 256 * 4 passes the check
+    assert call(lib, T=2 ** 24 // 64 * 64 // 1, H=1, G=1) == tcg.ATTN_EINVAL
+    big = call(lib, q=0x10000000000, k=0x20000000000, v=0x30000000000, o=0x40000000000,
+               l=0x50000000000, T=2 ** 24 - 64, H=1, G=1)
+    assert big != tcg.ATTN_EINVAL
+
+
+def test_rejects_null_pointers(lib):
+    assert call(lib, q=0) == tcg.ATTN_EINVAL
+    assert call(lib, l=0) == tcg.ATTN_EINVAL
+
+
+def test_rejects_misaligned_pointers(lib):
+    assert call(lib, q=0x1008) == tcg.ATTN_EALIGN
+    assert call(lib, o=0x300004) == tcg.ATTN_EALIGN
+
+
+def test_rejects_overlapping_outputs(lib):
+    # q occupies 4*128*64*2 = 65536 bytes from 0x1000
+    assert call(lib, o=0x1000 + 65536 - 16) == tcg.ATTN_EOVERLAP
+    assert call(lib, l=0x100000 + 16) == tcg.ATTN_EOVERLAP
+    assert call(lib, o=0x300000, l=0x300000 + 65536 - 16) == tcg.ATTN_EOVERLAP
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call(lib) == tcg.ATTN_EDEVICE
+
+
+def test_workspace_bytes(lib):
+    T, H, G = 8192, 32, 8
+    up = lambda n: (n + 255) // 256 * 256
+    want = up(H * T * 128) * 2 + up(G * T * 128) * 2 + up(H * T * 4)
+    assert tcg.attn_fwd_workspace_bytes(T, H, G) == want
+    assert tcg.attn_fwd_workspace_bytes(100, H, G) == 0
+
+
+def test_binding_checks_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(4, 128, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        tcg.attn_fwd(q, q, q, q, q, 128, 4, 2, 0.18)

@@ -1,0 +1,149 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Tolerances (written here, from the headline statement of the method's
+accuracy): max |dO| <= 4e-3 and max |dLSE| <= 1e-3 (base 2), elementwise, on
+the same seeded binary16 inputs.  Small and ragged shapes are compared on
+every element; the two largest workloads, in the launch configuration the
+benchmark times, on sampled rows the oracle computes one by one, plus
+properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import transformer_causal_gqa_gb300 as tcg
+from transformer_causal_gqa_gb300 import build as tcg_build
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 4e-3
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tcg_build.build()
+    return tcg.load_library()
+
+
+def run_gpu(q, k, vT, T, H, G, c, stream=None):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, vT))
+    o = torch.full((T, H * 64), float("nan"), dtype=torch.float16, device=dev)
+    lse = torch.full((H, T), float("nan"), dtype=torch.float32, device=dev)
+    tcg.attn_fwd(qd, kd, vd, o, lse, T, H, G, c, stream)
+    assert tcg.last_device_status(stream) == tcg.ATTN_OK
+    return o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def compare_full(w):
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    o, lse = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    d_o = float(np.abs(o - o_ref).max())
+    d_l = float(np.abs(lse - lse_ref).max())
+    assert d_o <= TOL_O, f"max |dO| = {d_o}"
+    assert d_l <= TOL_LSE, f"max |dLSE| = {d_l}"
+    return d_o, d_l
+
+
+@pytest.mark.parametrize("name", ["t128_h4_kv2", "t1024_h12_kv12_mha", "t2048_h16_kv4_peaked"])
+def test_workload_every_element(name):
+    compare_full(synthetic.WORKLOADS[name])
+
+
+# ragged tails: T mod 256 in {64, 128, 192, 0}; groups 1, 2, 4, 8
+@pytest.mark.parametrize("T", [64, 192, 320, 384, 448, 640, 1088])
+@pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1)])
+def test_shapes_every_element(T, H, G):
+    compare_full(synthetic.custom(T, H, G, seed=T * 100 + H * 10 + G))
+
+
+def test_outlier_keys_small():
+    compare_full(synthetic.custom(1152, 16, 2, seed=77, k_outlier_every=97,
+                                  k_outlier_scale=16.0, v_uniform=True))
+
+
+def test_peaked_many_heads():
+    compare_full(synthetic.custom(768, 32, 4, seed=78, qk_scale=4.0))
+
+
+def test_more_units_than_sms():
+    # 160 heads x 2 row blocks = 320 work units: each CTA takes several
+    compare_full(synthetic.custom(512, 160, 20, seed=79))
+
+
+def sample_rows(T, H, n_random, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 63, 64, 127, 128, 129, 255, 256, T // 2, T - 129, T - 128, T - 2, T - 1]
+    rows = np.concatenate([np.array(fixed), rng.integers(0, T, n_random)])
+    heads = np.concatenate([np.arange(len(fixed)) % H, rng.integers(0, H, n_random)])
+    extra_h = np.arange(H)                      # every head, its last row
+    return (np.concatenate([heads, extra_h]),
+            np.concatenate([rows, np.full(H, T - 1)]))
+
+
+@pytest.mark.parametrize("name,n_random", [("t8192_h32_kv8", 600), ("t16384_h64_kv8_outliers", 300)])
+def test_full_size_sampled_rows(name, n_random):
+    w = synthetic.WORKLOADS[name]
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    o, lse = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    # properties at every element: finite, LSE >= the row's first score's bound
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    vmax = float(np.abs(vT.astype(np.float32)).max())
+    assert float(np.abs(o).max()) <= vmax * (1 + 1e-3)   # a convex combination of V rows
+    hs, rs = sample_rows(w.T, w.heads, n_random, seed=w.seed)
+    o_ref, lse_ref = oracle.attn_fwd_rows(q, k, vT, w.T, w.heads, w.kv_heads, c, hs, rs)
+    got_o = np.stack([o[r, h * 64:(h + 1) * 64] for h, r in zip(hs, rs)])
+    got_l = lse[hs, rs]
+    d_o = float(np.abs(got_o - o_ref).max())
+    d_l = float(np.abs(got_l - lse_ref).max())
+    assert d_o <= TOL_O, f"max |dO| = {d_o}"
+    assert d_l <= TOL_LSE, f"max |dLSE| = {d_l}"
+
+
+def test_deterministic_and_stream():
+    w = synthetic.custom(1024, 8, 2, seed=80)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    s = torch.cuda.Stream()
+    a = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    with torch.cuda.stream(s):
+        b = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c, stream=s)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_host_entry_matches_device_entry():
+    w = synthetic.custom(640, 8, 4, seed=81)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    o_dev, lse_dev = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (q, k, vT))
+    oh = torch.empty((w.T, w.heads * 64), dtype=torch.float16).pin_memory()
+    lh = torch.empty((w.heads, w.T), dtype=torch.float32).pin_memory()
+    ws = torch.empty(tcg.attn_fwd_workspace_bytes(w.T, w.heads, w.kv_heads),
+                     dtype=torch.uint8, device="cuda")
+    tcg.attn_fwd_host(qh, kh, vh, oh, lh, w.T, w.heads, w.kv_heads, c, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(oh.numpy().astype(np.float64), o_dev)
+    assert np.array_equal(lh.numpy().astype(np.float64), lse_dev)
+
+
+def test_rejections_on_device():
+    dev = torch.device("cuda:0")
+    q = torch.zeros(4, 128, 64, dtype=torch.float16, device=dev)
+    k = torch.zeros(2, 128, 64, dtype=torch.float16, device=dev)
+    vT = torch.zeros(2, 64, 128, dtype=torch.float16, device=dev)
+    lse = torch.zeros(4, 128, dtype=torch.float32, device=dev)
+    # o aliasing q is refused before anything is queued
+    with pytest.raises(tcg.AttnError) as e:
+        tcg.attn_fwd(q, k, vT, q.view(128, 256), lse, 128, 4, 2, 0.18)
+    assert e.value.status == tcg.ATTN_EOVERLAP
+    assert tcg.last_device_status() == tcg.ATTN_OK

@@ -1,0 +1,153 @@
+"""GB300 (sm_103a) causal grouped-query attention forward, streaming normalised sum.
+
+A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h``
+(``libattn_gb300.so``): it checks tensor dtypes, devices and contiguity, and
+passes raw pointers, sizes and the stream handle.  Every step of the forward
+pass runs in the library's CUDA kernel; there is no CPU path.  If the library
+has not been built, every entry point raises ``RuntimeError``.
+
+Layouts (the page "Realization/Nvidia/SM86/StreamingAttentionSM86.alpha"):
+q binary16 [heads][T][64], k binary16 [kv_heads][T][64], vT binary16
+[kv_heads][64][T]; outputs o binary16 [T][heads*64] and lse binary32
+[heads][T] (base-2 log-sum-exp).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+HEAD_DIM = 64
+
+ATTN_OK = 0
+ATTN_EINVAL = -1
+ATTN_EALIGN = -2
+ATTN_EOVERLAP = -3
+ATTN_ELAUNCH = -4
+ATTN_EDEVICE = -5
+ATTN_ETIMEOUT = -6
+
+# every symbol include/attn_fwd.h declares
+EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
+            "attn_last_device_status", "attn_status_string")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Loads libattn_gb300.so (built by ``transformer_causal_gqa_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m transformer_causal_gqa_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_fwd_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_fwd_workspace_bytes.restype = sz
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp, sz, vp]
+    lib.attn_fwd_host.restype = i
+    lib.attn_last_device_status.argtypes = [vp]
+    lib.attn_last_device_status.restype = i
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+def _check_tensor(name, t, dtype, shape, device=True):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if device and t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not device and t.device.type != "cpu":
+        raise ValueError(f"{name}: must be a host tensor")
+    del torch
+
+
+def attn_fwd(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float, stream=None) -> None:
+    """Forward pass on CUDA tensors, queued on ``stream`` (default: torch's current)."""
+    import torch
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T))
+    _check_tensor("o", o, torch.float16, (T, heads * HEAD_DIM))
+    _check_tensor("lse", lse, torch.float32, (heads, T))
+    rc = load_library().attn_fwd(q.data_ptr(), k.data_ptr(), vT.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), int(T), int(heads), int(kv_heads),
+                                 float(c), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+
+
+def attn_fwd_workspace_bytes(T: int, heads: int, kv_heads: int) -> int:
+    return int(load_library().attn_fwd_workspace_bytes(int(T), int(heads), int(kv_heads)))
+
+
+def attn_fwd_host(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
+                  workspace, stream=None) -> None:
+    """Forward pass on host tensors (pinned for asynchronous copies); ``workspace``
+    is a CUDA uint8 tensor of at least attn_fwd_workspace_bytes bytes.  Queued on
+    ``stream``; synchronise it before reading o and lse."""
+    import torch
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM), device=False)
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM), device=False)
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T), device=False)
+    _check_tensor("o", o, torch.float16, (T, heads * HEAD_DIM), device=False)
+    _check_tensor("lse", lse, torch.float32, (heads, T), device=False)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace: must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().attn_fwd_host(q.data_ptr(), k.data_ptr(), vT.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), int(T), int(heads), int(kv_heads),
+                                      float(c), workspace.data_ptr(), nbytes,
+                                      _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronises ``stream``; ATTN_OK, or ATTN_ETIMEOUT if a kernel wait gave up."""
+    return int(load_library().attn_last_device_status(_stream_handle(stream)))
+
+
+def attention(q, k, vT, c: float, stream=None):
+    """Allocates o and lse with torch and runs attn_fwd; returns (o, lse)."""
+    import torch
+    heads, T, _ = q.shape
+    kv_heads = k.shape[0]
+    o = torch.empty((T, heads * HEAD_DIM), dtype=torch.float16, device=q.device)
+    lse = torch.empty((heads, T), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, vT, o, lse, T, heads, kv_heads, c, stream)
+    return o, lse

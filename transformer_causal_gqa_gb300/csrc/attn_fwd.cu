@@ -1,0 +1,631 @@
+// attn_fwd.cu -- causal grouped-query attention forward for GB300 (sm_103a),
+// computed as a streaming normalised sum, behind the C ABI of attn_fwd.h.
+//
+// What it computes is the forward pass described in the header comment of
+// "Realization/Nvidia/SM86/StreamingAttentionSM86.alpha": scores in base-2
+// units t = S c, a running row maximum m, running sum l and running weighted
+// sum O folded tile by tile (a new maximum m' scales the old l and O by
+// 2^(m - m')), the weights 2^(t - m) rounded to binary16 only for their
+// product with V, O / l written binary16 token-major and m + log2 l written
+// binary32 per head.  Only the tiles up to and including the diagonal one are
+// visited, and only the diagonal tile is masked (key column > query row).
+//
+// How (GB300-first, not the page's SM86 register-fragment design):
+//   * a persistent grid, one CTA per SM, walks work units of 256 query rows
+//     of one head (two 128-row subtiles sharing every K/V^T tile), heaviest
+//     (latest) row blocks first in a serpentine order across the CTAs;
+//   * one warp issues TMA loads: Q subtiles and a ring of 16 KiB K and V^T
+//     tiles (128 keys x 64), 128-byte swizzled, signalled by mbarriers;
+//   * one thread issues tcgen05 MMAs: S = Q K^T (M=128, N=128, K=64) into
+//     tensor memory, then O += P V (M=128, N=64, K=128) with P read from
+//     tensor memory where the softmax wrote it over S;
+//   * two softmax warpgroups, one per subtile, one thread per query row:
+//     tcgen05.ld the row's 128 scores, mask, row maximum, exp2, row sum,
+//     round P to binary16 and tcgen05.st it back; rescale O in tensor memory
+//     when the maximum rose; at the end normalise and store O and the LSE.
+//   Subtile 0's softmax overlaps subtile 1's MMAs and vice versa.
+//
+// Every wait on an mbarrier is bounded in time; on expiry the CTA records
+// ATTN_ETIMEOUT in a device status word, drains what it has in flight, frees
+// its tensor memory and exits.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_fwd.h"
+#include "sm103_ptx.cuh"
+
+namespace {
+
+using namespace sm103;
+
+constexpr int kHeadDim = 64;
+constexpr int kBlockM = 128;              // query rows per subtile = TMEM lanes
+constexpr int kUnitRows = 2 * kBlockM;    // query rows per work unit
+constexpr int kBlockN = 128;              // keys per K / V^T tile
+constexpr int kStages = 6;                // ring slots
+constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // 16 KiB: a K tile, a V^T tile, a Q subtile
+constexpr int kThreads = 320;             // 8 softmax warps, MMA warp, TMA warp
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: S/P of subtile s at 128 s, O of subtile s at 256 + 64 s
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+
+// dynamic shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
+constexpr int kNumBars = 2 + 2 * kStages + 7;
+constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
+constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
+
+// barrier indices
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = 1;
+constexpr int kBarKvFull = 2;                   // + slot
+constexpr int kBarKvEmpty = 2 + kStages;        // + slot
+constexpr int kBarSFull = 2 + 2 * kStages;      // + subtile
+constexpr int kBarPFull = kBarSFull + 2;        // + subtile
+constexpr int kBarOFull = kBarPFull + 2;        // + subtile
+constexpr int kBarDrain = kBarOFull + 2;        // MMA issuer's own drain on abort
+
+struct Params {
+  int T;
+  int heads;
+  int group;          // query heads per K/V head
+  int row_blocks;     // ceil(T / 256)
+  int units;          // heads * row_blocks
+  float c;
+  __half *o;
+  float *lse;
+  int *status;
+};
+
+struct Unit {
+  int h, g, b;        // query head, K/V head, row block
+  int row0;           // first query row
+  int n0, n1;         // key tiles visited by subtile 0 and subtile 1
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
+  Unit w;
+  const int rb = u / p.heads;
+  w.h = u - rb * p.heads;
+  w.b = p.row_blocks - 1 - rb;          // latest row blocks (most tiles) first
+  w.g = w.h / p.group;
+  w.row0 = w.b * kUnitRows;
+  const int end = min(p.T, w.row0 + kUnitRows);
+  w.n0 = 2 * w.b + 1;                   // subtile 0: tiles 0 .. its diagonal 2b
+  w.n1 = (end + kBlockN - 1) / kBlockN; // subtile 1: through 2b+1, or 2b when it holds no row < T
+  return w;
+}
+
+// k-th unit of this CTA, serpentine across the grid; -1 when done.
+__device__ __forceinline__ int unit_of(int k, const Params &p) {
+  const int G = gridDim.x;
+  const int slot = (k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int u = k * G + slot;
+  return u < p.units ? u : -1;
+}
+
+struct Sync {
+  uint32_t bar0;              // smem address of barrier 0
+  volatile int *abort_flag;   // smem
+  int *status;                // global
+  __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+
+  // Bounded wait: false if the CTA is aborting or the wait ran out of time.
+  __device__ bool wait(int i, uint32_t parity, int where) const {
+    const uint32_t b = bar(i);
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait(b, parity)) return true;
+      if ((it & 63u) == 0) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicCAS(status, 0, where);
+          return false;
+        }
+      }
+    }
+  }
+
+  // While aborting: wait for this thread's own copies or MMAs in flight,
+  // bounded in time only.
+  __device__ void drain_wait(int i, uint32_t parity) const {
+    const uint32_t b = bar(i);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, parity))
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+  }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ----------------------------------------------------------------------------
+// TMA warp (one lane): Q subtiles, then K(j), V^T(j) for j = 0 .. n1-1.
+__device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                          const Params &p, const Sync &sy, uint32_t smem) {
+  uint32_t pos = 0;         // running ring position (K and V^T tiles alternate)
+  uint32_t pos_issued = 0;  // ring positions whose copy has been issued
+  uint32_t q_issued = 0;    // Q loads issued
+  int k = 0;
+  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+    const Unit w = decode_unit(u, p);
+    if (!sy.wait(kBarQEmpty, (k & 1) ^ 1, 1)) goto drain;
+    ++q_issued;
+    mbar_arrive_expect_tx(sy.bar(kBarQFull), 2 * kTileBytes);
+    tma_load_3d(smem + kOffQ, tmQ, sy.bar(kBarQFull), 0, w.row0, w.h);
+    tma_load_3d(smem + kOffQ + kTileBytes, tmQ, sy.bar(kBarQFull), 0, w.row0 + kBlockM, w.h);
+    for (int j = 0; j < w.n1; ++j) {
+      for (int kv = 0; kv < 2; ++kv, ++pos) {
+        const uint32_t slot = pos % kStages;
+        if (!sy.wait(kBarKvEmpty + slot, ((pos / kStages) & 1) ^ 1, 2)) goto drain;
+        const uint32_t dst = smem + kOffRing + slot * kTileBytes;
+        const uint32_t full = sy.bar(kBarKvFull + slot);
+        mbar_arrive_expect_tx(full, kTileBytes);
+        pos_issued = pos + 1;
+        if (kv == 0) {
+          tma_load_3d(dst, tmK, full, 0, j * kBlockN, w.g);
+        } else {
+          tma_load_3d(dst, tmV, full, j * kBlockN, 0, w.g);
+          tma_load_3d(dst + kTileBytes / 2, tmV, full, j * kBlockN + kBlockN / 2, 0, w.g);
+        }
+      }
+    }
+  }
+  return;
+drain:
+  // Aborting: let the copies already issued land before the CTA exits.
+  for (uint32_t i = 0; i < kStages && i < pos_issued; ++i) {
+    const uint32_t q = pos_issued - 1 - i;
+    sy.drain_wait(kBarKvFull + q % kStages, (q / kStages) & 1);
+  }
+  if (q_issued > 0) sy.drain_wait(kBarQFull, (q_issued - 1) & 1);
+}
+
+// ----------------------------------------------------------------------------
+// MMA issuer (one thread).
+__device__ void mma_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
+  constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
+  constexpr uint32_t idPV = idesc_f16_f32(kBlockM, kHeadDim);
+  uint32_t pos = 0;
+  uint32_t pphase[2] = {0, 0};
+  int k = 0;
+  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+    const Unit w = decode_unit(u, p);
+    const int nt[2] = {w.n0, w.n1};
+    int v_ready = 0;  // V^T tiles of this unit already waited for
+    auto ensure_v = [&](int j) -> bool {
+      for (; v_ready <= j; ++v_ready) {
+        const uint32_t q = pos + 2 * v_ready + 1;
+        if (!sy.wait(kBarKvFull + q % kStages, (q / kStages) & 1, 10)) return false;
+      }
+      return true;
+    };
+    // O_s += P_s V(j); frees V(j)'s slot after its last reader.
+    auto issue_pv = [&](int s, int j) {
+      const uint32_t vslot = (pos + 2 * j + 1) % kStages;
+      const uint32_t vbase = smem + kOffRing + vslot * kTileBytes;
+      const uint32_t pcol = tmem + kColS + 128u * s;
+#pragma unroll
+      for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        const uint64_t bdesc = sw128_desc(vbase + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+        mma_ts(tmem + kColO + 64u * s, pcol + 8u * kk, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      const bool deferred0 = (j == w.n0 - 1) && (w.n1 > w.n0);
+      const bool last_reader = (s == 1) ? !deferred0 : deferred0;
+      if (last_reader) mma_commit(sy.bar(kBarKvEmpty + vslot));
+    };
+
+    if (!sy.wait(kBarQFull, k & 1, 11)) goto drain;
+    tc_fence_after();
+    for (int j = 0; j < w.n1; ++j) {
+      const uint32_t kpos = pos + 2 * j;
+      const uint32_t kslot = kpos % kStages;
+      if (!sy.wait(kBarKvFull + kslot, (kpos / kStages) & 1, 12)) goto drain;
+      tc_fence_after();
+      const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
+      for (int s = 0; s < 2; ++s) {
+        if (j >= nt[s]) continue;
+        if (j > 0) {
+          // softmax s has written P_s(j-1) and rescaled O_s
+          if (!sy.wait(kBarPFull + s, pphase[s], 13)) goto drain;
+          pphase[s] ^= 1;
+          tc_fence_after();
+          if (!ensure_v(j - 1)) goto drain;
+          issue_pv(s, j - 1);
+        }
+        const uint32_t qbase = smem + kOffQ + s * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_ss(tmem + kColS + 128u * s, sw128_desc(qbase + kk * 32), sw128_desc(kbase + kk * 32),
+                 idS, kk > 0 ? 1u : 0u);
+        mma_commit(sy.bar(kBarSFull + s));
+      }
+      mma_commit(sy.bar(kBarKvEmpty + kslot));  // K(j) read by both subtiles' S
+    }
+    mma_commit(sy.bar(kBarQEmpty));  // every S of this unit issued
+    for (int s = 0; s < 2; ++s) {
+      const int j = nt[s] - 1;
+      if (!sy.wait(kBarPFull + s, pphase[s], 14)) goto drain;
+      pphase[s] ^= 1;
+      tc_fence_after();
+      if (!ensure_v(j)) goto drain;
+      issue_pv(s, j);
+      mma_commit(sy.bar(kBarOFull + s));
+    }
+    pos += 2 * w.n1;
+  }
+  return;
+drain:
+  // Aborting: wait until the MMAs already issued have finished.
+  mma_commit(sy.bar(kBarDrain));
+  sy.drain_wait(kBarDrain, 0);
+}
+
+// ----------------------------------------------------------------------------
+// Softmax warpgroup for subtile s: thread r owns query row r (TMEM lane r).
+__device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tmem) {
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_base = (uint32_t)((threadIdx.x & 96)) << 16;  // warp's 32-lane slice
+  const uint32_t tS = tmem + lane_base + kColS + 128u * s;
+  const uint32_t tO = tmem + lane_base + kColO + 64u * s;
+  const float c = p.c;
+  uint32_t sphase = 0, ophase = 0;
+  int k = 0;
+  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+    const Unit w = decode_unit(u, p);
+    const int n = s ? w.n1 : w.n0;
+    const int diag = 2 * w.b + s;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < n; ++j) {
+      if (!sy.wait(kBarSFull + s, sphase, 20 + s)) return;
+      sphase ^= 1;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      float sv[128];
+#pragma unroll
+      for (int col = 0; col < kBlockN; ++col) sv[col] = __uint_as_float(sr[col]);
+      if (j == diag) {
+#pragma unroll
+        for (int col = 0; col < kBlockN; ++col)
+          if (col > r) sv[col] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int col = 1; col < kBlockN; ++col) mx = fmaxf(mx, sv[col]);
+      const float m_new = fmaxf(m_run, mx * c);
+      const float alpha = ex2(m_run - m_new);
+      const float neg = -m_new;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2(fmaf(sv[2 * i], c, neg));
+        const float p1 = ex2(fmaf(sv[2 * i + 1], c, neg));
+        sum += p0 + p1;
+        pk[i] = pack_half2(p0, p1);
+      }
+      l_run = l_run * alpha + sum;
+      tmem_st_x64(tS, pk);
+      // O_s holds P V through tile j-1 (complete: S_s(j) was committed after it)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        uint32_t orow[64];
+        tmem_ld_x64(tO, orow);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+        tmem_st_x64(tO, orow);
+      }
+      tc_fence_before();
+      mbar_arrive(sy.bar(kBarPFull + s));
+      m_run = m_new;
+    }
+    // epilogue: O / l and m + log2 l once the last P V is done
+    if (!sy.wait(kBarOFull + s, ophase, 22 + s)) return;
+    ophase ^= 1;
+    tc_fence_after();
+    uint32_t orow[64];
+    tmem_ld_x64(tO, orow);
+    const int row = w.row0 + s * kBlockM + r;
+    if (row < p.T) {
+      const float inv = 1.f / l_run;
+      uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)row * p.heads + w.h) * kHeadDim);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint4 v;
+        v.x = pack_half2(__uint_as_float(orow[8 * i + 0]) * inv, __uint_as_float(orow[8 * i + 1]) * inv);
+        v.y = pack_half2(__uint_as_float(orow[8 * i + 2]) * inv, __uint_as_float(orow[8 * i + 3]) * inv);
+        v.z = pack_half2(__uint_as_float(orow[8 * i + 4]) * inv, __uint_as_float(orow[8 * i + 5]) * inv);
+        v.w = pack_half2(__uint_as_float(orow[8 * i + 6]) * inv, __uint_as_float(orow[8 * i + 7]) * inv);
+        dst[i] = v;
+      }
+      p.lse[(size_t)w.h * p.T + row] = m_run + log2f(l_run);
+    }
+    tc_fence_before();  // O's reads are ordered before the next unit's first P V
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t smem = (raw + 1023u) & ~1023u;
+  uint8_t *smem_gen = smem_raw + (smem - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  Sync sy;
+  sy.bar0 = smem + kOffBar;
+  sy.abort_flag = reinterpret_cast<volatile int *>(smem_gen + kOffAbort);
+  sy.status = p.status;
+
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    mbar_init(sy.bar(kBarQFull), 1);
+    mbar_init(sy.bar(kBarQEmpty), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(sy.bar(kBarKvFull + i), 1);
+      mbar_init(sy.bar(kBarKvEmpty + i), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sy.bar(kBarSFull + s), 1);
+      mbar_init(sy.bar(kBarPFull + s), kBlockM);
+      mbar_init(sy.bar(kBarOFull + s), 1);
+    }
+    mbar_init(sy.bar(kBarDrain), 1);
+    *sy.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem + kOffTmemPtr, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
+
+  if (warp < 8) {
+    softmax_role(warp >> 2, p, sy, tmem);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role(p, sy, smem, tmem);
+    __syncwarp();
+  } else if (warp == kLoadWarp) {
+    if (lane == 0) load_role(&tmQ, &tmK, &tmV, p, sy, smem);
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ============================================================================
+// host side
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int *status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return ATTN_EDEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState &st = g_dev[dev];
+  if (!st.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_EDEVICE;
+    if (prop.major != 10 || prop.minor != 3) return ATTN_EDEVICE;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void *fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return ATTN_ELAUNCH;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return ATTN_ELAUNCH;
+    if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+    if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+    st.sms = prop.multiProcessorCount;
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// The page's admission predicate for the forward program, plus c.
+int check_shape(int T, int heads, int kv_heads, float c) {
+  if (T <= 0 || heads <= 0 || kv_heads <= 0) return ATTN_EINVAL;
+  if (T % 64 != 0) return ATTN_EINVAL;
+  if (heads % kv_heads != 0) return ATTN_EINVAL;
+  if (heads > ATTN_MAX_HEADS) return ATTN_EINVAL;
+  if ((uint64_t)heads * 64u * (uint64_t)T * 4u > 0xFFFFFFFFull) return ATTN_EINVAL;
+  if (!std::isfinite(c) || !(c > 0.f)) return ATTN_EINVAL;
+  return ATTN_OK;
+}
+
+struct Sizes {
+  size_t q, kv, o, lse;
+};
+Sizes sizes_of(int T, int heads, int kv_heads) {
+  Sizes z;
+  z.q = (size_t)heads * T * kHeadDim * 2;
+  z.kv = (size_t)kv_heads * T * kHeadDim * 2;
+  z.o = z.q;
+  z.lse = (size_t)heads * T * 4;
+  return z;
+}
+
+int check_args(const void *q, const void *k, const void *vT, const void *o, const void *lse, int T,
+               int heads, int kv_heads, float c) {
+  const int rc = check_shape(T, heads, kv_heads, c);
+  if (rc) return rc;
+  if (!q || !k || !vT || !o || !lse) return ATTN_EINVAL;
+  for (const void *ptr : {q, k, vT, o, lse})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return ATTN_EALIGN;
+  const Sizes z = sizes_of(T, heads, kv_heads);
+  if (overlaps(o, z.o, lse, z.lse)) return ATTN_EOVERLAP;
+  for (const void *out : {o, lse}) {
+    const size_t n = out == o ? z.o : z.lse;
+    if (overlaps(out, n, q, z.q) || overlaps(out, n, k, z.kv) || overlaps(out, n, vT, z.kv))
+      return ATTN_EOVERLAP;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, float *lse, int T,
+                        int heads, int kv_heads, float c, cudaStream_t stream) {
+  int rc = check_args(q, k, vT, o, lse, T, heads, kv_heads, c);
+  if (rc) return rc;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t rowb = kHeadDim * 2;
+  if (!encode_3d(&tmQ, q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
+      !encode_3d(&tmK, k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
+      !encode_3d(&tmV, vT, T, kHeadDim, kv_heads, (uint64_t)T * 2, (uint64_t)T * 2 * kHeadDim,
+                 kBlockN / 2, kHeadDim))
+    return ATTN_ELAUNCH;
+
+  Params p;
+  p.T = T;
+  p.heads = heads;
+  p.group = heads / kv_heads;
+  p.row_blocks = (T + kUnitRows - 1) / kUnitRows;
+  p.units = heads * p.row_blocks;
+  p.c = c;
+  p.o = static_cast<__half *>(o);
+  p.lse = lse;
+  p.status = st->status;
+  const int grid = p.units < st->sms ? p.units : st->sms;
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  return ATTN_OK;
+}
+
+extern "C" size_t attn_fwd_workspace_bytes(int T, int heads, int kv_heads) {
+  if (check_shape(T, heads, kv_heads, 1.f)) return 0;
+  const Sizes z = sizes_of(T, heads, kv_heads);
+  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+  return up(z.q) + 2 * up(z.kv) + up(z.o) + up(z.lse);
+}
+
+extern "C" int attn_fwd_host(const void *q, const void *k, const void *vT, void *o, float *lse,
+                             int T, int heads, int kv_heads, float c, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(T, heads, kv_heads, c);
+  if (rc) return rc;
+  if (!q || !k || !vT || !o || !lse || !workspace) return ATTN_EINVAL;
+  if (workspace_bytes < attn_fwd_workspace_bytes(T, heads, kv_heads)) return ATTN_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_EALIGN;
+  const Sizes z = sizes_of(T, heads, kv_heads);
+  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint8_t *dq = ws, *dk = dq + up(z.q), *dv = dk + up(z.kv), *dout = dv + up(z.kv),
+          *dlse = dout + up(z.o);
+  if (cudaMemcpyAsync(dq, q, z.q, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k, z.kv, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dv, vT, z.kv, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ELAUNCH;
+  }
+  rc = attn_fwd(dq, dk, dv, dout, reinterpret_cast<float *>(dlse), T, heads, kv_heads, c, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(o, dout, z.o, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(lse, dlse, z.lse, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ELAUNCH;
+  }
+  return ATTN_OK;
+}
+
+extern "C" int attn_last_device_status(cudaStream_t stream) {
+  DeviceState *st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ELAUNCH;
+  int word = 0;
+  if (cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  if (word != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+  return word ? ATTN_ETIMEOUT : ATTN_OK;
+}
+
+extern "C" const char *attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_EINVAL: return "invalid argument (shape, scale or null pointer)";
+    case ATTN_EALIGN: return "pointer not 16-byte aligned";
+    case ATTN_EOVERLAP: return "an output overlaps an input or the other output";
+    case ATTN_ELAUNCH: return "CUDA runtime refused a copy, the set-up or the launch";
+    case ATTN_EDEVICE: return "no sm_103 (GB300) CUDA device is current";
+    case ATTN_ETIMEOUT: return "a kernel wait timed out; outputs are not valid";
+    default: return "unknown status";
+  }
+}
