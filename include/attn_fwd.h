@@ -107,6 +107,35 @@ int attn_fwd_host(const void *q, const void *k, const void *vT, void *o, float *
  */
 int attn_last_device_status(cudaStream_t stream);
 
+/*
+ * attn_fwd_noalloc -- attn_fwd for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart of this entry point; it exists for
+ * callers such as runtimes that plan every device byte ahead of time and
+ * forbid allocation once running, processes held to a fixed device-memory
+ * quota, and latency-critical loops that cannot afford cudaMalloc's implicit
+ * device synchronisation.  attn_fwd allocates one 4-byte status word per
+ * device on its first call; this variant instead keeps the kernel's scratch
+ * (that status word) in a fixed 256-byte array compiled into the library, so
+ * it calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layouts, admission checks and results are those of attn_fwd.
+ * status: NULL, or a host or device pointer that receives (ordered on
+ *   `stream`) the kernel's status word: 0 if every wait inside the kernel
+ *   completed, non-zero if one gave up (then o and lse are not valid).
+ *
+ * The scratch this kernel needs does not depend on the shape (4 bytes); the
+ * call returns ATTN_EINVAL if it ever exceeded the array's 256 bytes.
+ * The first call on each device looks up the array's device address and
+ * sets the kernel's shared-memory attribute: make that first call before any
+ * stream capture.  Each call clears the status word (it keeps the previous
+ * call's value until then).  Every call on every stream shares the one array,
+ * so calls that overlap on the GPU race on the status word.
+ */
+int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, float *lse,
+                     int T, int heads, int kv_heads, float c, int *status,
+                     cudaStream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *attn_status_string(int status);
 

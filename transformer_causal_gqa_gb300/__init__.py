@@ -30,7 +30,7 @@ ATTN_ETIMEOUT = -6
 
 # every symbol include/attn_fwd.h declares
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
-            "attn_last_device_status", "attn_status_string")
+            "attn_last_device_status", "attn_fwd_noalloc", "attn_status_string")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load_library():
     lib.attn_fwd_host.restype = i
     lib.attn_last_device_status.argtypes = [vp]
     lib.attn_last_device_status.restype = i
+    lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp, vp]
+    lib.attn_fwd_noalloc.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -135,6 +137,28 @@ def attn_fwd_host(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
                                       _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_host")
+
+
+def attn_fwd_noalloc(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
+                     status=None, stream=None) -> None:
+    """attn_fwd without any device allocation: the kernel's status word lives in a
+    fixed array inside the library.  ``status``: None, or a 1-element int32 tensor
+    (host or CUDA) that receives the word (0 = every kernel wait completed) in
+    stream order.  Calls that overlap on the GPU share the word."""
+    import torch
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T))
+    _check_tensor("o", o, torch.float16, (T, heads * HEAD_DIM))
+    _check_tensor("lse", lse, torch.float32, (heads, T))
+    if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
+        raise TypeError("status: expected an int32 tensor with at least one element")
+    rc = load_library().attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), vT.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), int(T), int(heads), int(kv_heads),
+                                         float(c), None if status is None else status.data_ptr(),
+                                         _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_noalloc")
 
 
 def last_device_status(stream=None) -> int:

@@ -617,6 +617,109 @@ extern "C" int attn_last_device_status(cudaStream_t stream) {
   return word ? ATTN_ETIMEOUT : ATTN_OK;
 }
 
+// ============================================================================
+// attn_fwd_noalloc: the same kernel with its scratch (the status word) in a
+// fixed array compiled into this library instead of a cudaMalloc'd word.
+
+// 256 bytes (64 words), held by every GPU that loads this library until the
+// process exits; the kernel needs one word of it.  Host code must not use
+// this name as a device address: it gets the address from cudaGetSymbolAddress.
+static __device__ __align__(256) int g_noalloc_scratch[64];
+
+namespace {
+
+struct NoAllocState {
+  bool ready = false;
+  int sms = 0;
+  int *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[64];
+
+// Once per device, with that device current: checks the device, sets the
+// kernel's shared-memory attribute and looks up the array's device address.
+int noalloc_state(NoAllocState **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return ATTN_EDEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  NoAllocState &st = g_noalloc[dev];
+  if (!st.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_EDEVICE;
+    if (prop.major != 10 || prop.minor != 3) return ATTN_EDEVICE;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void *fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return ATTN_ELAUNCH;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return ATTN_ELAUNCH;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return ATTN_ELAUNCH;
+    }
+    st.scratch = static_cast<int *>(ptr);
+    st.sms = prop.multiProcessorCount;
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, float *lse,
+                                int T, int heads, int kv_heads, float c, int *status,
+                                cudaStream_t stream) {
+  int rc = check_args(q, k, vT, o, lse, T, heads, kv_heads, c);
+  if (rc) return rc;
+  const size_t scratch_needed = sizeof(int);  // the status word, for every shape
+  if (scratch_needed > sizeof(g_noalloc_scratch)) return ATTN_EINVAL;
+  NoAllocState *st = nullptr;
+  if ((rc = noalloc_state(&st))) return rc;
+
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t rowb = kHeadDim * 2;
+  if (!encode_3d(&tmQ, q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
+      !encode_3d(&tmK, k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
+      !encode_3d(&tmV, vT, T, kHeadDim, kv_heads, (uint64_t)T * 2, (uint64_t)T * 2 * kHeadDim,
+                 kBlockN / 2, kHeadDim))
+    return ATTN_ELAUNCH;
+
+  Params p;
+  p.T = T;
+  p.heads = heads;
+  p.group = heads / kv_heads;
+  p.row_blocks = (T + kUnitRows - 1) / kUnitRows;
+  p.units = heads * p.row_blocks;
+  p.c = c;
+  p.o = static_cast<__half *>(o);
+  p.lse = lse;
+  p.status = st->scratch;
+  // the array keeps the previous call's word: the kernel only ever sets it from 0
+  if (cudaMemsetAsync(st->scratch, 0, scratch_needed, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ELAUNCH;
+  }
+  const int grid = p.units < st->sms ? p.units : st->sms;
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  if (status && cudaMemcpyAsync(status, st->scratch, sizeof(int), cudaMemcpyDefault, stream) !=
+                    cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ELAUNCH;
+  }
+  return ATTN_OK;
+}
+
 extern "C" const char *attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ok";
