@@ -52,19 +52,23 @@ constexpr int kUnitRows = 2 * kBlockM;    // query rows per work unit
 constexpr int kBlockN = 128;              // keys per K / V^T tile
 constexpr int kStages = 6;                // ring slots
 constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // 16 KiB: a K tile, a V^T tile, a Q subtile
-constexpr int kThreads = 320;             // 8 softmax warps, MMA warp, TMA warp
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 384;             // 8 softmax warps, 3 MMA-issuing warps, TMA warp
+constexpr int kSWarp = 8;                 // issues S = Q K^T for both subtiles
+constexpr int kPvWarp0 = 9;               // issues O_s += P_s V for subtile s = warp - kPvWarp0
+constexpr int kLoadWarp = 11;
+static_assert(kStages % 2 == 0, "K tiles must land in even ring slots, V^T tiles in odd ones");
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: S/P of subtile s at 128 s, O of subtile s at 256 + 64 s
+// tensor-memory columns: S of subtile s at 128 s, O at 256 + 64 s, P (binary16
+// pairs) at 384 + 64 s -- all 512 columns
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
-constexpr int kNumBars = 2 + 2 * kStages + 7;
+constexpr int kNumBars = 2 + 2 * kStages + 11;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemUsed = kOffAbort + 4;
@@ -77,10 +81,11 @@ constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
 constexpr int kBarKvFull = 2;                   // + slot
 constexpr int kBarKvEmpty = 2 + kStages;        // + slot
-constexpr int kBarSFull = 2 + 2 * kStages;      // + subtile
-constexpr int kBarPFull = kBarSFull + 2;        // + subtile
-constexpr int kBarOFull = kBarPFull + 2;        // + subtile
-constexpr int kBarDrain = kBarOFull + 2;        // MMA issuer's own drain on abort
+constexpr int kBarSFull = 2 + 2 * kStages;      // + subtile: S_s computed
+constexpr int kBarSFree = kBarSFull + 2;        // + subtile: S_s read into registers
+constexpr int kBarPFull = kBarSFree + 2;        // + subtile: P_s written, O_s rescaled
+constexpr int kBarPvDone = kBarPFull + 2;       // + subtile: O_s += P_s V complete
+constexpr int kBarDrain = kBarPvDone + 2;       // + MMA warp (0..2): its own drain on abort
 
 struct Params {
   int T;
@@ -145,6 +150,12 @@ struct Sync {
     }
   }
 
+  // Bounded wait taken by a whole warp: every lane gets the same answer.
+  __device__ bool wait_warp(int i, uint32_t parity, int where) const {
+    const bool ok = wait(i, parity, where);
+    return __all_sync(0xffffffffu, ok);
+  }
+
   // While aborting: wait for this thread's own copies or MMAs in flight,
   // bounded in time only.
   __device__ void drain_wait(int i, uint32_t parity) const {
@@ -164,6 +175,46 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c), two IEEE fmas in one instruction.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1), two IEEE adds in one instruction.
+__device__ __forceinline__ void add2(float &s0, float &s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rs;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rs, {%0, %1};\n\t"
+      "add.f32x2 rs, rs, ra;\n\t"
+      "mov.b64 {%0, %1}, rs;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
+// (d0, d1) = (a0 * b, a1 * b), two IEEE multiplies in one instruction.
+__device__ __forceinline__ void mul2(float &d0, float &d1, float b) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\t"
+      "mov.b64 rb, {%2, %2};\n\t"
+      "mul.f32x2 ra, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(b));
 }
 
 // ----------------------------------------------------------------------------
@@ -209,57 +260,34 @@ drain:
 }
 
 // ----------------------------------------------------------------------------
-// MMA issuer (one thread).
-__device__ void mma_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
+// The tensor pipe takes a new tcgen05.mma from a given warp only every ~100
+// cycles, so three warps issue concurrently: one for S = Q K^T (both
+// subtiles, 4 MMAs of N = 128 per tile each) and one per subtile for
+// O += P V (8 MMAs of N = 64 per tile, A = P read from tensor memory).
+// Each accumulation chain is issued by a single warp, so it stays ordered.
+
+// S issuer: S_s(j) as soon as the softmax has pulled S_s(j-1) into registers.
+__device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
-  constexpr uint32_t idPV = idesc_f16_f32(kBlockM, kHeadDim);
   uint32_t pos = 0;
-  uint32_t pphase[2] = {0, 0};
+  uint32_t s_issued[2] = {0, 0};  // S MMAs issued per subtile (S-free is an "empty" barrier)
   int k = 0;
   for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
     const Unit w = decode_unit(u, p);
-    const int nt[2] = {w.n0, w.n1};
-    int v_ready = 0;  // V^T tiles of this unit already waited for
-    auto ensure_v = [&](int j) -> bool {
-      for (; v_ready <= j; ++v_ready) {
-        const uint32_t q = pos + 2 * v_ready + 1;
-        if (!sy.wait(kBarKvFull + q % kStages, (q / kStages) & 1, 10)) return false;
-      }
-      return true;
-    };
-    // O_s += P_s V(j); frees V(j)'s slot after its last reader.
-    auto issue_pv = [&](int s, int j) {
-      const uint32_t vslot = (pos + 2 * j + 1) % kStages;
-      const uint32_t vbase = smem + kOffRing + vslot * kTileBytes;
-      const uint32_t pcol = tmem + kColS + 128u * s;
-#pragma unroll
-      for (int kk = 0; kk < kBlockN / 16; ++kk) {
-        const uint64_t bdesc = sw128_desc(vbase + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
-        mma_ts(tmem + kColO + 64u * s, pcol + 8u * kk, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      const bool deferred0 = (j == w.n0 - 1) && (w.n1 > w.n0);
-      const bool last_reader = (s == 1) ? !deferred0 : deferred0;
-      if (last_reader) mma_commit(sy.bar(kBarKvEmpty + vslot));
-    };
-
-    if (!sy.wait(kBarQFull, k & 1, 11)) goto drain;
+    if (!sy.wait_warp(kBarQFull, k & 1, 11)) goto drain;
     tc_fence_after();
     for (int j = 0; j < w.n1; ++j) {
       const uint32_t kpos = pos + 2 * j;
       const uint32_t kslot = kpos % kStages;
-      if (!sy.wait(kBarKvFull + kslot, (kpos / kStages) & 1, 12)) goto drain;
+      if (!sy.wait_warp(kBarKvFull + kslot, (kpos / kStages) & 1, 12)) goto drain;
       tc_fence_after();
       const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
+#pragma unroll
       for (int s = 0; s < 2; ++s) {
-        if (j >= nt[s]) continue;
-        if (j > 0) {
-          // softmax s has written P_s(j-1) and rescaled O_s
-          if (!sy.wait(kBarPFull + s, pphase[s], 13)) goto drain;
-          pphase[s] ^= 1;
-          tc_fence_after();
-          if (!ensure_v(j - 1)) goto drain;
-          issue_pv(s, j - 1);
-        }
+        if (j >= (s ? w.n1 : w.n0)) continue;
+        if (!sy.wait_warp(kBarSFree + s, (s_issued[s] & 1) ^ 1, 13)) goto drain;
+        ++s_issued[s];
+        tc_fence_after();
         const uint32_t qbase = smem + kOffQ + s * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
@@ -270,33 +298,63 @@ __device__ void mma_role(const Params &p, const Sync &sy, uint32_t smem, uint32_
       mma_commit(sy.bar(kBarKvEmpty + kslot));  // K(j) read by both subtiles' S
     }
     mma_commit(sy.bar(kBarQEmpty));  // every S of this unit issued
-    for (int s = 0; s < 2; ++s) {
-      const int j = nt[s] - 1;
-      if (!sy.wait(kBarPFull + s, pphase[s], 14)) goto drain;
-      pphase[s] ^= 1;
-      tc_fence_after();
-      if (!ensure_v(j)) goto drain;
-      issue_pv(s, j);
-      mma_commit(sy.bar(kBarOFull + s));
+    pos += 2 * w.n1;
+  }
+  return;
+drain:
+  mma_commit(sy.bar(kBarDrain + 0));
+  sy.drain_wait(kBarDrain + 0, 0);
+}
+
+// P V issuer for subtile s: O_s += P_s(j) V(j) once the softmax has written P_s(j).
+// It releases every V^T tile of the unit (the barrier counts both subtiles'
+// issuers), including the one subtile 0 does not read when n1 > n0.
+__device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
+  constexpr uint32_t idPV = idesc_f16_f32(kBlockM, kHeadDim);
+  uint32_t pos = 0;
+  uint32_t pphase = 0;
+  int k = 0;
+  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+    const Unit w = decode_unit(u, p);
+    const int n = s ? w.n1 : w.n0;
+    for (int j = 0; j < w.n1; ++j) {
+      const uint32_t vpos = pos + 2 * j + 1;
+      const uint32_t vslot = vpos % kStages;
+      if (j < n) {
+        if (!sy.wait_warp(kBarPFull + s, pphase, 14)) goto drain;
+        pphase ^= 1;
+        if (!sy.wait_warp(kBarKvFull + vslot, (vpos / kStages) & 1, 10)) goto drain;
+        tc_fence_after();
+        const uint32_t vbase = smem + kOffRing + vslot * kTileBytes;
+        const uint32_t pcol = tmem + kColP + 64u * s;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = sw128_desc(vbase + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+          mma_ts(tmem + kColO + 64u * s, pcol + 8u * kk, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(sy.bar(kBarPvDone + s));
+      }
+      mma_commit(sy.bar(kBarKvEmpty + vslot));
     }
     pos += 2 * w.n1;
   }
   return;
 drain:
-  // Aborting: wait until the MMAs already issued have finished.
-  mma_commit(sy.bar(kBarDrain));
-  sy.drain_wait(kBarDrain, 0);
+  mma_commit(sy.bar(kBarDrain + 1 + s));
+  sy.drain_wait(kBarDrain + 1 + s, 0);
 }
 
 // ----------------------------------------------------------------------------
 // Softmax warpgroup for subtile s: thread r owns query row r (TMEM lane r).
 __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tmem) {
   const int r = threadIdx.x & 127;
+  const bool leader = (threadIdx.x & 31) == 0;
   const uint32_t lane_base = (uint32_t)((threadIdx.x & 96)) << 16;  // warp's 32-lane slice
   const uint32_t tS = tmem + lane_base + kColS + 128u * s;
   const uint32_t tO = tmem + lane_base + kColO + 64u * s;
+  const uint32_t tP = tmem + lane_base + kColP + 64u * s;
   const float c = p.c;
-  uint32_t sphase = 0, ophase = 0;
+  uint32_t sphase = 0, pvphase = 0;
   int k = 0;
   for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
     const Unit w = decode_unit(u, p);
@@ -304,11 +362,15 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
     const int diag = 2 * w.b + s;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n; ++j) {
-      if (!sy.wait(kBarSFull + s, sphase, 20 + s)) return;
+      if (!sy.wait_warp(kBarSFull + s, sphase, 20 + s)) return;
       sphase ^= 1;
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
+      // S_s is in registers: the tensor pipe may overwrite it with S_s(j+1)
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarSFree + s));
       float sv[128];
 #pragma unroll
       for (int col = 0; col < kBlockN; ++col) sv[col] = __uint_as_float(sr[col]);
@@ -317,39 +379,60 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
         for (int col = 0; col < kBlockN; ++col)
           if (col > r) sv[col] = -INFINITY;
       }
-      float mx = sv[0];
+      // row maximum: eight independent chains of 3-input max
+      float mx8[8];
 #pragma unroll
-      for (int col = 1; col < kBlockN; ++col) mx = fmaxf(mx, sv[col]);
+      for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(sv[a], sv[8 + a]);
+#pragma unroll
+      for (int col = 16; col < kBlockN; col += 16)
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = max3(mx8[a], sv[col + a], sv[col + 8 + a]);
+      const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
+                            fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_run, mx * c);
       const float alpha = ex2(m_run - m_new);
       const float neg = -m_new;
-      float sum = 0.f;
+      // P = 2^(S c - m'): paired fmas, exp2 on the SFU, paired row sums
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2(fmaf(sv[2 * i], c, neg));
-        const float p1 = ex2(fmaf(sv[2 * i + 1], c, neg));
-        sum += p0 + p1;
+        float t0, t1;
+        fma2(t0, t1, sv[2 * i], sv[2 * i + 1], c, neg);
+        const float p0 = ex2(t0);
+        const float p1 = ex2(t1);
+        add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
         pk[i] = pack_half2(p0, p1);
       }
+      const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       l_run = l_run * alpha + sum;
-      tmem_st_x64(tS, pk);
-      // O_s holds P V through tile j-1 (complete: S_s(j) was committed after it)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        uint32_t orow[64];
-        tmem_ld_x64(tO, orow);
+      if (j > 0) {
+        // P_s(j-1) V(j-1) must be complete before O_s is rescaled and P_s is overwritten
+        if (!sy.wait_warp(kBarPvDone + s, pvphase, 24 + s)) return;
+        pvphase ^= 1;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t orow[64];
+          tmem_ld_x64(tO, orow);
+          float of[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-        tmem_st_x64(tO, orow);
+          for (int i = 0; i < 64; ++i) of[i] = __uint_as_float(orow[i]);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) mul2(of[i], of[i + 1], alpha);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) orow[i] = __float_as_uint(of[i]);
+          tmem_st_x64(tO, orow);
+        }
       }
+      tmem_st_x64(tP, pk);
       tc_fence_before();
-      mbar_arrive(sy.bar(kBarPFull + s));
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarPFull + s));
       m_run = m_new;
     }
     // epilogue: O / l and m + log2 l once the last P V is done
-    if (!sy.wait(kBarOFull + s, ophase, 22 + s)) return;
-    ophase ^= 1;
+    if (!sy.wait_warp(kBarPvDone + s, pvphase, 22 + s)) return;
+    pvphase ^= 1;
     tc_fence_after();
     uint32_t orow[64];
     tmem_ld_x64(tO, orow);
@@ -395,18 +478,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sy.bar(kBarQEmpty), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(sy.bar(kBarKvFull + i), 1);
-      mbar_init(sy.bar(kBarKvEmpty + i), 1);
+      // K slots are released by the S issuer, V^T slots by both P V issuers
+      mbar_init(sy.bar(kBarKvEmpty + i), (i % 2 == 0) ? 1 : 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sy.bar(kBarSFull + s), 1);
-      mbar_init(sy.bar(kBarPFull + s), kBlockM);
-      mbar_init(sy.bar(kBarOFull + s), 1);
+      mbar_init(sy.bar(kBarSFree + s), kBlockM / 32);  // one arrival per softmax warp
+      mbar_init(sy.bar(kBarPFull + s), kBlockM / 32);
+      mbar_init(sy.bar(kBarPvDone + s), 1);
     }
-    mbar_init(sy.bar(kBarDrain), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(sy.bar(kBarDrain + i), 1);
     *sy.abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tmem_alloc(smem + kOffTmemPtr, kTmemCols);
     tmem_relinquish();
   }
@@ -417,9 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     softmax_role(warp >> 2, p, sy, tmem);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role(p, sy, smem, tmem);
-    __syncwarp();
+  } else if (warp == kSWarp) {
+    s_role(p, sy, smem, tmem);
+  } else if (warp == kPvWarp0 || warp == kPvWarp0 + 1) {
+    pv_role(warp - kPvWarp0, p, sy, smem, tmem);
   } else if (warp == kLoadWarp) {
     if (lane == 0) load_role(&tmQ, &tmK, &tmV, p, sy, smem);
     __syncwarp();
@@ -427,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
