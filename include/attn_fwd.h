@@ -24,9 +24,11 @@
  *   o    binary16 [T][heads*64]        (token-major, heads merged)  -- output
  *   lse  binary32 [heads][T]           (base-2 log-sum-exp)          -- output
  *
- * Ownership: the caller owns every buffer.  The library keeps, per device,
- * one 4-byte status word it allocates on first use and never frees; it
- * allocates nothing per call.
+ * Ownership: the caller owns every buffer.  The library keeps, per device, a
+ * 384-byte scratch block it allocates on first use and never frees (a status
+ * word and 32 slots of work counters the kernel's dynamic tile scheduler
+ * uses, one slot per launch in rotation); it allocates nothing per call.
+ * More than 32 launches in flight on the GPU at once would share a slot.
  *
  * Errors: every entry point returns an attn_status.  Argument errors are
  * detected on the host before anything is launched.  The launches are
@@ -114,23 +116,25 @@ int attn_last_device_status(cudaStream_t stream);
  * callers such as runtimes that plan every device byte ahead of time and
  * forbid allocation once running, processes held to a fixed device-memory
  * quota, and latency-critical loops that cannot afford cudaMalloc's implicit
- * device synchronisation.  attn_fwd allocates one 4-byte status word per
- * device on its first call; this variant instead keeps the kernel's scratch
- * (that status word) in a fixed 256-byte array compiled into the library, so
- * it calls no cudaMalloc, cudaFree or other allocating routine.
+ * device synchronisation.  attn_fwd allocates a scratch block per device on
+ * its first call; this variant instead keeps the kernel's scratch (a status
+ * word and 16 slots of work counters for the tile scheduler) in a fixed
+ * 256-byte array compiled into the library, so it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
  *
  * Arguments, layouts, admission checks and results are those of attn_fwd.
  * status: NULL, or a host or device pointer that receives (ordered on
  *   `stream`) the kernel's status word: 0 if every wait inside the kernel
  *   completed, non-zero if one gave up (then o and lse are not valid).
  *
- * The scratch this kernel needs does not depend on the shape (4 bytes); the
+ * The scratch this kernel needs does not depend on the shape (192 bytes); the
  * call returns ATTN_EINVAL if it ever exceeded the array's 256 bytes.
  * The first call on each device looks up the array's device address and
  * sets the kernel's shared-memory attribute: make that first call before any
- * stream capture.  Each call clears the status word (it keeps the previous
- * call's value until then).  Every call on every stream shares the one array,
- * so calls that overlap on the GPU race on the status word.
+ * stream capture.  Each call clears the status word and its counter slot
+ * (they keep the previous call's values until then).  Every call on every
+ * stream shares the one array: calls that overlap on the GPU race on the
+ * status word, and on a counter slot when more than 16 are in flight.
  */
 int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, float *lse,
                      int T, int heads, int kv_heads, float c, int *status,

@@ -50,12 +50,14 @@ constexpr int kHeadDim = 64;
 constexpr int kBlockM = 128;              // query rows per subtile = TMEM lanes
 constexpr int kUnitRows = 2 * kBlockM;    // query rows per work unit
 constexpr int kBlockN = 128;              // keys per K / V^T tile
-constexpr int kStages = 6;                // ring slots
+constexpr int kStages = 6;                // K / V^T ring slots
 constexpr uint32_t kTileBytes = kBlockN * kHeadDim * 2;  // 16 KiB: a K tile, a V^T tile, a Q subtile
 constexpr int kThreads = 384;             // 8 softmax warps, 3 MMA-issuing warps, TMA warp
 constexpr int kSWarp = 8;                 // issues S = Q K^T for both subtiles
 constexpr int kPvWarp0 = 9;               // issues O_s += P_s V for subtile s = warp - kPvWarp0
 constexpr int kLoadWarp = 11;
+constexpr int kConsumerWarps = 11;        // every warp but the TMA warp reads the unit queue
+constexpr int kUnitSlots = 4;             // unit queue depth
 static_assert(kStages % 2 == 0, "K tiles must land in even ring slots, V^T tiles in odd ones");
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: S of subtile s at 128 s, O at 256 + 64 s, P (binary16
@@ -64,28 +66,37 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;
 
+// barrier indices
+constexpr int kBarQFull = 0;                    // + Q buffer (2)
+constexpr int kBarQEmpty = 2;                   // + Q buffer
+constexpr int kBarKvFull = 4;                   // + ring slot
+constexpr int kBarKvEmpty = kBarKvFull + kStages;
+constexpr int kBarSFull = kBarKvEmpty + kStages;  // + subtile: S_s computed
+constexpr int kBarSFree = kBarSFull + 2;        // + subtile: S_s read into registers
+constexpr int kBarPFull = kBarSFree + 2;        // + subtile: P_s written, O_s rescaled
+constexpr int kBarPvDone = kBarPFull + 2;       // + subtile: O_s += P_s V complete
+constexpr int kBarUnitFull = kBarPvDone + 2;    // + queue slot: a unit id published
+constexpr int kBarUnitEmpty = kBarUnitFull + kUnitSlots;  // + queue slot: read by every consumer
+constexpr int kBarDrain = kBarUnitEmpty + kUnitSlots;     // + MMA warp (0..2): its own drain on abort
+constexpr int kNumBars = kBarDrain + 3;
+
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffQ = 0;                               // 2 buffers x 2 subtiles
+constexpr uint32_t kOffRing = 4 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
-constexpr int kNumBars = 2 + 2 * kStages + 11;
-constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffUnits = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffTmemPtr = kOffUnits + kUnitSlots * 4;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemUsed = kOffAbort + 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
 
-// barrier indices
-constexpr int kBarQFull = 0;
-constexpr int kBarQEmpty = 1;
-constexpr int kBarKvFull = 2;                   // + slot
-constexpr int kBarKvEmpty = 2 + kStages;        // + slot
-constexpr int kBarSFull = 2 + 2 * kStages;      // + subtile: S_s computed
-constexpr int kBarSFree = kBarSFull + 2;        // + subtile: S_s read into registers
-constexpr int kBarPFull = kBarSFree + 2;        // + subtile: P_s written, O_s rescaled
-constexpr int kBarPvDone = kBarPFull + 2;       // + subtile: O_s += P_s V complete
-constexpr int kBarDrain = kBarPvDone + 2;       // + MMA warp (0..2): its own drain on abort
+// Device scratch the kernel uses beyond its inputs and outputs: a status
+// word, and a ring of work-counter slots (next unit, finished CTAs), one slot
+// per launch so that launches overlapping on different streams do not share one.
+constexpr int kScratchStatus = 0;
+constexpr int kScratchSched = 32;         // first counter slot (2 ints per slot)
 
 struct Params {
   int T;
@@ -97,6 +108,7 @@ struct Params {
   __half *o;
   float *lse;
   int *status;
+  int *sched;         // this launch's counter slot: [0] next unit, [1] CTAs done
 };
 
 struct Unit {
@@ -105,11 +117,12 @@ struct Unit {
   int n0, n1;         // key tiles visited by subtile 0 and subtile 1
 };
 
+// Unit u in order of decreasing cost: the latest row blocks (most key tiles) first.
 __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
   Unit w;
   const int rb = u / p.heads;
   w.h = u - rb * p.heads;
-  w.b = p.row_blocks - 1 - rb;          // latest row blocks (most tiles) first
+  w.b = p.row_blocks - 1 - rb;
   w.g = w.h / p.group;
   w.row0 = w.b * kUnitRows;
   const int end = min(p.T, w.row0 + kUnitRows);
@@ -118,17 +131,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
   return w;
 }
 
-// k-th unit of this CTA, serpentine across the grid; -1 when done.
-__device__ __forceinline__ int unit_of(int k, const Params &p) {
-  const int G = gridDim.x;
-  const int slot = (k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int u = k * G + slot;
-  return u < p.units ? u : -1;
-}
-
 struct Sync {
   uint32_t bar0;              // smem address of barrier 0
   volatile int *abort_flag;   // smem
+  volatile int *units;        // smem unit queue
   int *status;                // global
   __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * i; }
 
@@ -163,6 +169,18 @@ struct Sync {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(b, parity))
       if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+  }
+
+  // The k-th unit this CTA works on, read by a whole consumer warp from the
+  // queue the TMA warp fills: a unit id, -1 when the work is exhausted, -2 if
+  // the CTA is aborting.
+  __device__ int next_unit(int k) const {
+    const int slot = k % kUnitSlots;
+    if (!wait_warp(kBarUnitFull + slot, (k / kUnitSlots) & 1, 30)) return -2;
+    const int u = units[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
+    return u;
   }
 };
 
@@ -218,26 +236,36 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float b) {
 }
 
 // ----------------------------------------------------------------------------
-// TMA warp (one lane): Q subtiles, then K(j), V^T(j) for j = 0 .. n1-1.
+// TMA warp (one lane): takes units from the global work counter and publishes
+// them to the CTA's unit queue; for each, loads the two Q subtiles into the
+// unit's Q buffer, then K(j), V^T(j) for j = 0 .. n1-1 through the ring.
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const Params &p, const Sync &sy, uint32_t smem) {
   uint32_t pos = 0;         // running ring position (K and V^T tiles alternate)
   uint32_t pos_issued = 0;  // ring positions whose copy has been issued
   uint32_t q_issued = 0;    // Q loads issued
-  int k = 0;
-  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+  for (int k = 0;; ++k) {
+    const int slot = k % kUnitSlots;
+    if (!sy.wait(kBarUnitEmpty + slot, ((k / kUnitSlots) & 1) ^ 1, 1)) goto drain;
+    int u = atomicAdd(&p.sched[0], 1);
+    if (u >= p.units) u = -1;
+    sy.units[slot] = u;
+    mbar_arrive(sy.bar(kBarUnitFull + slot));
+    if (u < 0) break;
     const Unit w = decode_unit(u, p);
-    if (!sy.wait(kBarQEmpty, (k & 1) ^ 1, 1)) goto drain;
+    const int qb = k & 1;
+    if (!sy.wait(kBarQEmpty + qb, ((k >> 1) & 1) ^ 1, 1)) goto drain;
     ++q_issued;
-    mbar_arrive_expect_tx(sy.bar(kBarQFull), 2 * kTileBytes);
-    tma_load_3d(smem + kOffQ, tmQ, sy.bar(kBarQFull), 0, w.row0, w.h);
-    tma_load_3d(smem + kOffQ + kTileBytes, tmQ, sy.bar(kBarQFull), 0, w.row0 + kBlockM, w.h);
+    const uint32_t qdst = smem + kOffQ + qb * 2 * kTileBytes;
+    mbar_arrive_expect_tx(sy.bar(kBarQFull + qb), 2 * kTileBytes);
+    tma_load_3d(qdst, tmQ, sy.bar(kBarQFull + qb), 0, w.row0, w.h);
+    tma_load_3d(qdst + kTileBytes, tmQ, sy.bar(kBarQFull + qb), 0, w.row0 + kBlockM, w.h);
     for (int j = 0; j < w.n1; ++j) {
       for (int kv = 0; kv < 2; ++kv, ++pos) {
-        const uint32_t slot = pos % kStages;
-        if (!sy.wait(kBarKvEmpty + slot, ((pos / kStages) & 1) ^ 1, 2)) goto drain;
-        const uint32_t dst = smem + kOffRing + slot * kTileBytes;
-        const uint32_t full = sy.bar(kBarKvFull + slot);
+        const uint32_t rs = pos % kStages;
+        if (!sy.wait(kBarKvEmpty + rs, ((pos / kStages) & 1) ^ 1, 2)) goto drain;
+        const uint32_t dst = smem + kOffRing + rs * kTileBytes;
+        const uint32_t full = sy.bar(kBarKvFull + rs);
         mbar_arrive_expect_tx(full, kTileBytes);
         pos_issued = pos + 1;
         if (kv == 0) {
@@ -249,6 +277,12 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
       }
     }
   }
+  // This CTA takes no more units.  The last CTA to get here resets the
+  // launch's counter slot for the next launch that uses it.
+  if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
+    atomicExch(&p.sched[0], 0);
+    atomicExch(&p.sched[1], 0);
+  }
   return;
 drain:
   // Aborting: let the copies already issued land before the CTA exits.
@@ -256,7 +290,10 @@ drain:
     const uint32_t q = pos_issued - 1 - i;
     sy.drain_wait(kBarKvFull + q % kStages, (q / kStages) & 1);
   }
-  if (q_issued > 0) sy.drain_wait(kBarQFull, (q_issued - 1) & 1);
+  for (uint32_t i = 0; i < 2 && i < q_issued; ++i) {
+    const uint32_t q = q_issued - 1 - i;
+    sy.drain_wait(kBarQFull + (q & 1), (q >> 1) & 1);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -271,10 +308,13 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
   constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
   uint32_t pos = 0;
   uint32_t s_issued[2] = {0, 0};  // S MMAs issued per subtile (S-free is an "empty" barrier)
-  int k = 0;
-  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+  for (int k = 0;; ++k) {
+    const int u = sy.next_unit(k);
+    if (u == -1) return;
+    if (u < 0) goto drain;
     const Unit w = decode_unit(u, p);
-    if (!sy.wait_warp(kBarQFull, k & 1, 11)) goto drain;
+    const int qb = k & 1;
+    if (!sy.wait_warp(kBarQFull + qb, (k >> 1) & 1, 11)) goto drain;
     tc_fence_after();
     for (int j = 0; j < w.n1; ++j) {
       const uint32_t kpos = pos + 2 * j;
@@ -288,7 +328,7 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
         if (!sy.wait_warp(kBarSFree + s, (s_issued[s] & 1) ^ 1, 13)) goto drain;
         ++s_issued[s];
         tc_fence_after();
-        const uint32_t qbase = smem + kOffQ + s * kTileBytes;
+        const uint32_t qbase = smem + kOffQ + (qb * 2 + s) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           mma_ss(tmem + kColS + 128u * s, sw128_desc(qbase + kk * 32), sw128_desc(kbase + kk * 32),
@@ -297,10 +337,9 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
       }
       mma_commit(sy.bar(kBarKvEmpty + kslot));  // K(j) read by both subtiles' S
     }
-    mma_commit(sy.bar(kBarQEmpty));  // every S of this unit issued
+    mma_commit(sy.bar(kBarQEmpty + qb));  // every S of this unit issued
     pos += 2 * w.n1;
   }
-  return;
 drain:
   mma_commit(sy.bar(kBarDrain + 0));
   sy.drain_wait(kBarDrain + 0, 0);
@@ -313,8 +352,10 @@ __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, u
   constexpr uint32_t idPV = idesc_f16_f32(kBlockM, kHeadDim);
   uint32_t pos = 0;
   uint32_t pphase = 0;
-  int k = 0;
-  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+  for (int k = 0;; ++k) {
+    const int u = sy.next_unit(k);
+    if (u == -1) return;
+    if (u < 0) goto drain;
     const Unit w = decode_unit(u, p);
     const int n = s ? w.n1 : w.n0;
     for (int j = 0; j < w.n1; ++j) {
@@ -338,7 +379,6 @@ __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, u
     }
     pos += 2 * w.n1;
   }
-  return;
 drain:
   mma_commit(sy.bar(kBarDrain + 1 + s));
   sy.drain_wait(kBarDrain + 1 + s, 0);
@@ -355,8 +395,9 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
   const uint32_t tP = tmem + lane_base + kColP + 64u * s;
   const float c = p.c;
   uint32_t sphase = 0, pvphase = 0;
-  int k = 0;
-  for (int u = unit_of(0, p); u >= 0; u = unit_of(++k, p)) {
+  for (int k = 0;; ++k) {
+    const int u = sy.next_unit(k);
+    if (u < 0) return;
     const Unit w = decode_unit(u, p);
     const int n = s ? w.n1 : w.n0;
     const int diag = 2 * w.b + s;
@@ -392,17 +433,18 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
       const float m_new = fmaxf(m_run, mx * c);
       const float alpha = ex2(m_run - m_new);
       const float neg = -m_new;
-      // P = 2^(S c - m'): paired fmas, exp2 on the SFU, paired row sums
+      // P = 2^(S c - m'), in three dense passes so the SFU sees 128 back-to-back
+      // exp2: paired fmas, then exp2, then paired row sums and binary16 packing
+#pragma unroll
+      for (int i = 0; i < 64; ++i) fma2(sv[2 * i], sv[2 * i + 1], sv[2 * i], sv[2 * i + 1], c, neg);
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = ex2(sv[i]);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        float t0, t1;
-        fma2(t0, t1, sv[2 * i], sv[2 * i + 1], c, neg);
-        const float p0 = ex2(t0);
-        const float p1 = ex2(t1);
-        add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
-        pk[i] = pack_half2(p0, p1);
+        add2(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], sv[2 * i], sv[2 * i + 1]);
+        pk[i] = pack_half2(sv[2 * i], sv[2 * i + 1]);
       }
       const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       l_run = l_run * alpha + sum;
@@ -411,6 +453,7 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
         if (!sy.wait_warp(kBarPvDone + s, pvphase, 24 + s)) return;
         pvphase ^= 1;
         tc_fence_after();
+        // the maximum rose for some row of this warp: O *= 2^(m - m') (alpha = 1 elsewhere)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t orow[64];
           tmem_ld_x64(tO, orow);
@@ -421,10 +464,11 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
           for (int i = 0; i < 64; i += 2) mul2(of[i], of[i + 1], alpha);
 #pragma unroll
           for (int i = 0; i < 64; ++i) orow[i] = __float_as_uint(of[i]);
-          tmem_st_x64(tO, orow);
+          tmem_st_x64_async(tO, orow);
         }
       }
-      tmem_st_x64(tP, pk);
+      tmem_st_x64_async(tP, pk);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarPFull + s));
@@ -468,14 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   Sync sy;
   sy.bar0 = smem + kOffBar;
   sy.abort_flag = reinterpret_cast<volatile int *>(smem_gen + kOffAbort);
+  sy.units = reinterpret_cast<volatile int *>(smem_gen + kOffUnits);
   sy.status = p.status;
 
   if (warp == kLoadWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    mbar_init(sy.bar(kBarQFull), 1);
-    mbar_init(sy.bar(kBarQEmpty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sy.bar(kBarQFull + b), 1);
+      mbar_init(sy.bar(kBarQEmpty + b), 1);
+    }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(sy.bar(kBarKvFull + i), 1);
       // K slots are released by the S issuer, V^T slots by both P V issuers
@@ -486,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sy.bar(kBarSFree + s), kBlockM / 32);  // one arrival per softmax warp
       mbar_init(sy.bar(kBarPFull + s), kBlockM / 32);
       mbar_init(sy.bar(kBarPvDone + s), 1);
+    }
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(sy.bar(kBarUnitFull + i), 1);
+      mbar_init(sy.bar(kBarUnitEmpty + i), kConsumerWarps);
     }
     for (int i = 0; i < 3; ++i) mbar_init(sy.bar(kBarDrain + i), 1);
     *sy.abort_flag = 0;
@@ -522,10 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 // host side
 
+constexpr int kSchedSlots = 32;           // counter slots in attn_fwd's scratch
+constexpr int kScratchInts = kScratchSched + 2 * kSchedSlots;
+
 struct DeviceState {
   bool ready = false;
   int sms = 0;
-  int *status = nullptr;
+  int *scratch = nullptr;     // kScratchInts ints: status word, then the counter slots
+  unsigned calls = 0;         // launches so far; picks the counter slot
 };
 
 std::mutex g_mutex;
@@ -556,8 +611,8 @@ int device_state(DeviceState **out) {
     if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return ATTN_ELAUNCH;
-    if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
-    if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+    if (cudaMalloc(&st.scratch, kScratchInts * sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+    if (cudaMemset(st.scratch, 0, kScratchInts * sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
     st.sms = prop.multiProcessorCount;
     st.ready = true;
   }
@@ -622,6 +677,26 @@ int check_args(const void *q, const void *k, const void *vT, const void *o, cons
   return ATTN_OK;
 }
 
+// Encodes the three tensor maps and fills the kernel parameters (all but the scratch).
+bool prepare(const void *q, const void *k, const void *vT, void *o, float *lse, int T, int heads,
+             int kv_heads, float c, CUtensorMap *tm, Params *p) {
+  const uint64_t rowb = kHeadDim * 2;
+  if (!encode_3d(&tm[0], q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
+      !encode_3d(&tm[1], k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
+      !encode_3d(&tm[2], vT, T, kHeadDim, kv_heads, (uint64_t)T * 2, (uint64_t)T * 2 * kHeadDim,
+                 kBlockN / 2, kHeadDim))
+    return false;
+  p->T = T;
+  p->heads = heads;
+  p->group = heads / kv_heads;
+  p->row_blocks = (T + kUnitRows - 1) / kUnitRows;
+  p->units = heads * p->row_blocks;
+  p->c = c;
+  p->o = static_cast<__half *>(o);
+  p->lse = lse;
+  return true;
+}
+
 }  // namespace
 
 extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, float *lse, int T,
@@ -630,27 +705,18 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, f
   if (rc) return rc;
   DeviceState *st = nullptr;
   if ((rc = device_state(&st))) return rc;
-
-  CUtensorMap tmQ, tmK, tmV;
-  const uint64_t rowb = kHeadDim * 2;
-  if (!encode_3d(&tmQ, q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
-      !encode_3d(&tmK, k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
-      !encode_3d(&tmV, vT, T, kHeadDim, kv_heads, (uint64_t)T * 2, (uint64_t)T * 2 * kHeadDim,
-                 kBlockN / 2, kHeadDim))
-    return ATTN_ELAUNCH;
-
+  CUtensorMap tm[3];
   Params p;
-  p.T = T;
-  p.heads = heads;
-  p.group = heads / kv_heads;
-  p.row_blocks = (T + kUnitRows - 1) / kUnitRows;
-  p.units = heads * p.row_blocks;
-  p.c = c;
-  p.o = static_cast<__half *>(o);
-  p.lse = lse;
-  p.status = st->status;
+  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, tm, &p)) return ATTN_ELAUNCH;
+  unsigned slot;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    slot = st->calls++ % kSchedSlots;
+  }
+  p.status = st->scratch + kScratchStatus;
+  p.sched = st->scratch + kScratchSched + 2 * slot;
   const int grid = p.units < st->sms ? p.units : st->sms;
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }
@@ -697,9 +763,12 @@ extern "C" int attn_last_device_status(cudaStream_t stream) {
   if (rc) return rc;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ELAUNCH;
   int word = 0;
-  if (cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&word, st->scratch + kScratchStatus, sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
     return ATTN_ELAUNCH;
-  if (word != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
+  // an aborted launch may also have left its work counters set: clear them all
+  if (word != 0 && cudaMemset(st->scratch, 0, kScratchInts * sizeof(int)) != cudaSuccess)
+    return ATTN_ELAUNCH;
   return word ? ATTN_ETIMEOUT : ATTN_OK;
 }
 
@@ -708,8 +777,11 @@ extern "C" int attn_last_device_status(cudaStream_t stream) {
 // fixed array compiled into this library instead of a cudaMalloc'd word.
 
 // 256 bytes (64 words), held by every GPU that loads this library until the
-// process exits; the kernel needs one word of it.  Host code must not use
-// this name as a device address: it gets the address from cudaGetSymbolAddress.
+// process exits: the status word at [0] and 16 work-counter slots of two words
+// from [32].  Host code must not use this name as a device address: it gets
+// the address from cudaGetSymbolAddress.
+constexpr int kNoAllocSchedSlots = 16;
+constexpr int kNoAllocScratchInts = kScratchSched + 2 * kNoAllocSchedSlots;
 static __device__ __align__(256) int g_noalloc_scratch[64];
 
 namespace {
@@ -718,6 +790,7 @@ struct NoAllocState {
   bool ready = false;
   int sms = 0;
   int *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  unsigned calls = 0;      // launches so far; picks the counter slot
 };
 NoAllocState g_noalloc[64];
 
@@ -767,38 +840,32 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, vo
                                 cudaStream_t stream) {
   int rc = check_args(q, k, vT, o, lse, T, heads, kv_heads, c);
   if (rc) return rc;
-  const size_t scratch_needed = sizeof(int);  // the status word, for every shape
+  // the scratch this kernel needs is the same for every shape
+  const size_t scratch_needed = kNoAllocScratchInts * sizeof(int);
   if (scratch_needed > sizeof(g_noalloc_scratch)) return ATTN_EINVAL;
   NoAllocState *st = nullptr;
   if ((rc = noalloc_state(&st))) return rc;
-
-  CUtensorMap tmQ, tmK, tmV;
-  const uint64_t rowb = kHeadDim * 2;
-  if (!encode_3d(&tmQ, q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
-      !encode_3d(&tmK, k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
-      !encode_3d(&tmV, vT, T, kHeadDim, kv_heads, (uint64_t)T * 2, (uint64_t)T * 2 * kHeadDim,
-                 kBlockN / 2, kHeadDim))
-    return ATTN_ELAUNCH;
-
+  CUtensorMap tm[3];
   Params p;
-  p.T = T;
-  p.heads = heads;
-  p.group = heads / kv_heads;
-  p.row_blocks = (T + kUnitRows - 1) / kUnitRows;
-  p.units = heads * p.row_blocks;
-  p.c = c;
-  p.o = static_cast<__half *>(o);
-  p.lse = lse;
-  p.status = st->scratch;
-  // the array keeps the previous call's word: the kernel only ever sets it from 0
-  if (cudaMemsetAsync(st->scratch, 0, scratch_needed, stream) != cudaSuccess) {
+  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, tm, &p)) return ATTN_ELAUNCH;
+  unsigned slot;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    slot = st->calls++ % kNoAllocSchedSlots;
+  }
+  p.status = st->scratch + kScratchStatus;
+  p.sched = st->scratch + kScratchSched + 2 * slot;
+  // the array keeps the previous call's contents: the kernel only ever sets the
+  // status word from 0, and counts units from a zeroed counter slot
+  if (cudaMemsetAsync(p.status, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), stream) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ELAUNCH;
   }
   const int grid = p.units < st->sms ? p.units : st->sms;
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-  if (status && cudaMemcpyAsync(status, st->scratch, sizeof(int), cudaMemcpyDefault, stream) !=
+  if (status && cudaMemcpyAsync(status, p.status, sizeof(int), cudaMemcpyDefault, stream) !=
                     cudaSuccess) {
     cudaGetLastError();
     return ATTN_ELAUNCH;
