@@ -53,7 +53,7 @@ typedef enum {
     ATTN_EOVERLAP = -3, /* an output overlaps an input or the other output */
     ATTN_ELAUNCH = -4,  /* the CUDA runtime refused a copy, the set-up or the launch */
     ATTN_EDEVICE = -5,  /* no current CUDA device, or it is not an sm_103 (GB300) part */
-    ATTN_ETIMEOUT = -6  /* a kernel wait gave up (reported by attn_last_device_status) */
+    ATTN_ETIMEOUT = -6  /* a kernel wait gave up after 1 s (reported by attn_last_device_status) */
 } attn_status;
 
 /* Largest number of query heads admitted (the page's limit of 65535). */
@@ -139,6 +139,19 @@ int attn_last_device_status(cudaStream_t stream);
 int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, float *lse,
                      int T, int heads, int kv_heads, float c, int *status,
                      cudaStream_t stream);
+
+/*
+ * attn_test_inject_stall -- test hook for the kernel's failure detection.
+ *
+ * The source pages have no counterpart of this entry point.  It makes the
+ * next attn_fwd launch in this process skip the first K-tile copy of its
+ * first CTA.  The wait on the missing tile then runs out after 1 s: the CTA
+ * records a timeout, drains the copies and MMAs it issued, frees its tensor
+ * memory and exits; attn_last_device_status then returns ATTN_ETIMEOUT (and
+ * clears the status word and the scheduler's counters), and later launches
+ * run normally.  Always returns ATTN_OK.  Only attn_fwd consumes the hook.
+ */
+int attn_test_inject_stall(void);
 
 /* A static, human-readable name for a status code. */
 const char *attn_status_string(int status);

@@ -1,0 +1,44 @@
+"""Failure detection on the GPU without a fault: a wait inside the kernel runs
+out (its tile is never loaded), the kernel reports ATTN_ETIMEOUT through the
+status word and exits cleanly, and the next launch is correct."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import transformer_causal_gqa_gb300 as tcg
+from transformer_causal_gqa_gb300 import build as tcg_build
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_runs_out_then_recovers():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tcg_build.build()
+    lib = tcg.load_library()
+    w = synthetic.custom(512, 4, 2, seed=31)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, vT))
+    o = torch.empty((w.T, w.heads * 64), dtype=torch.float16, device=dev)
+    lse = torch.empty((w.heads, w.T), dtype=torch.float32, device=dev)
+
+    assert tcg.last_device_status() == tcg.ATTN_OK
+    assert lib.attn_test_inject_stall() == tcg.ATTN_OK
+    t0 = time.monotonic()
+    tcg.attn_fwd(qd, kd, vd, o, lse, w.T, w.heads, w.kv_heads, c)
+    assert tcg.last_device_status() == tcg.ATTN_ETIMEOUT
+    assert time.monotonic() - t0 < 10.0         # bounded: a few 1 s waits at most
+    assert tcg.last_device_status() == tcg.ATTN_OK  # reading it cleared it
+
+    # the context is usable and the next launch is correct
+    tcg.attn_fwd(qd, kd, vd, o, lse, w.T, w.heads, w.kv_heads, c)
+    assert tcg.last_device_status() == tcg.ATTN_OK
+    o_ref, lse_ref = oracle.attn_fwd(q, k, vT, w.T, w.heads, w.kv_heads, c)
+    assert float(np.abs(o.cpu().numpy().astype(np.float64) - o_ref).max()) <= 4e-3
+    assert float(np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max()) <= 1e-3

@@ -30,7 +30,8 @@ ATTN_ETIMEOUT = -6
 
 # every symbol include/attn_fwd.h declares
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
-            "attn_last_device_status", "attn_fwd_noalloc", "attn_status_string")
+            "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
+            "attn_status_string")
 
 _lib = None
 
@@ -66,6 +67,8 @@ def load_library():
     lib.attn_last_device_status.restype = i
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp, vp]
     lib.attn_fwd_noalloc.restype = i
+    lib.attn_test_inject_stall.argtypes = []
+    lib.attn_test_inject_stall.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -90,7 +90,7 @@ constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemUsed = kOffAbort + 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
 
 // Device scratch the kernel uses beyond its inputs and outputs: a status
 // word, and a ring of work-counter slots (next unit, finished CTAs), one slot
@@ -239,6 +239,8 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float b) {
 // TMA warp (one lane): takes units from the global work counter and publishes
 // them to the CTA's unit queue; for each, loads the two Q subtiles into the
 // unit's Q buffer, then K(j), V^T(j) for j = 0 .. n1-1 through the ring.
+// kStallHook (test builds of the launch only): CTA 0 skips its first K tile, so a wait runs out.
+template <bool kStallHook>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const Params &p, const Sync &sy, uint32_t smem) {
   uint32_t pos = 0;         // running ring position (K and V^T tiles alternate)
@@ -266,8 +268,10 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         if (!sy.wait(kBarKvEmpty + rs, ((pos / kStages) & 1) ^ 1, 2)) goto drain;
         const uint32_t dst = smem + kOffRing + rs * kTileBytes;
         const uint32_t full = sy.bar(kBarKvFull + rs);
-        mbar_arrive_expect_tx(full, kTileBytes);
         pos_issued = pos + 1;
+        if (kStallHook && blockIdx.x == 0 && k == 0 && j == 0 && kv == 0)
+          continue;  // test hook: this K tile never arrives
+        mbar_arrive_expect_tx(full, kTileBytes);
         if (kv == 0) {
           tma_load_3d(dst, tmK, full, 0, j * kBlockN, w.g);
         } else {
@@ -499,6 +503,7 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
   }
 }
 
+template <bool kStallHook>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kPvWarp0 || warp == kPvWarp0 + 1) {
     pv_role(warp - kPvWarp0, p, sy, smem, tmem);
   } else if (warp == kLoadWarp) {
-    if (lane == 0) load_role(&tmQ, &tmK, &tmV, p, sy, smem);
+    if (lane == 0) load_role<kStallHook>(&tmQ, &tmK, &tmV, p, sy, smem);
     __syncwarp();
   }
 
@@ -584,6 +589,8 @@ struct DeviceState {
 };
 
 std::mutex g_mutex;
+// test hook: launches left to stall, and their wait bound
+int g_stall_launches = 0;
 DeviceState g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -608,7 +615,9 @@ int device_state(DeviceState **out) {
         return ATTN_ELAUNCH;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return ATTN_ELAUNCH;
     if (cudaMalloc(&st.scratch, kScratchInts * sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
@@ -709,14 +718,22 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, f
   Params p;
   if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, tm, &p)) return ATTN_ELAUNCH;
   unsigned slot;
+  bool stall = false;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     slot = st->calls++ % kSchedSlots;
+    if (g_stall_launches > 0) {
+      --g_stall_launches;
+      stall = true;
+    }
   }
   p.status = st->scratch + kScratchStatus;
   p.sched = st->scratch + kScratchSched + 2 * slot;
   const int grid = p.units < st->sms ? p.units : st->sms;
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+  if (stall)
+    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+  else
+    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }
@@ -817,7 +834,9 @@ int noalloc_state(NoAllocState **out) {
         return ATTN_ELAUNCH;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return ATTN_ELAUNCH;
     void *ptr = nullptr;
@@ -863,13 +882,19 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, vo
     return ATTN_ELAUNCH;
   }
   const int grid = p.units < st->sms ? p.units : st->sms;
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+  attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   if (status && cudaMemcpyAsync(status, p.status, sizeof(int), cudaMemcpyDefault, stream) !=
                     cudaSuccess) {
     cudaGetLastError();
     return ATTN_ELAUNCH;
   }
+  return ATTN_OK;
+}
+
+extern "C" int attn_test_inject_stall(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_stall_launches = 1;
   return ATTN_OK;
 }
 
