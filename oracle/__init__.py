@@ -62,6 +62,14 @@ def open_library(path: str):
     lib.oracle_attn_fwd_rows.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_float,
                                          i64p, i64p, i64, f64p, f64p, ctypes.c_int]
     lib.oracle_attn_fwd_rows.restype = ctypes.c_int
+    f = ctypes.c_float
+    lib.oracle_attn_bwd.argtypes = [u16p, u16p, u16p, f64p, f64p, u16p, i64, i64, i64, f, f,
+                                    f64p, f64p, f64p, f64p, ctypes.c_int]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
+    lib.oracle_attn_bwd_rows.argtypes = [u16p, u16p, u16p, f64p, f64p, u16p, i64, i64, i64, f, f,
+                                         i64p, i64p, i64, i64p, i64p, i64, f64p, f64p, f64p,
+                                         ctypes.c_int]
+    lib.oracle_attn_bwd_rows.restype = ctypes.c_int
     return lib
 
 
@@ -136,3 +144,70 @@ def attn_fwd_rows(q: np.ndarray, k: np.ndarray, vT: np.ndarray, T: int, heads: i
     if rc != 0:
         raise ValueError("oracle rejected the shape or an index")
     return o, lse
+
+
+def _f64(a, shape):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if a.shape != shape:
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a
+
+
+def attn_bwd(q, k, vT, o, lse, dO, T: int, heads: int, kv_heads: int, c: float, s: float,
+             threads: int = 0, lib=None):
+    """Backward pass.  o, lse: the forward's output and base-2 log-sum-exp (any float
+    dtype; taken as given); dO: binary16 [T][heads*64].  Returns (dQ [heads][T][64],
+    dK [kv_heads][T][64], dV^T [kv_heads][64][T], D [heads][T]), all float64."""
+    lib = lib or _load()
+    qb = _bits(q, (heads, T, HEAD_DIM))
+    kb = _bits(k, (kv_heads, T, HEAD_DIM))
+    vb = _bits(vT, (kv_heads, HEAD_DIM, T))
+    gb = _bits(dO, (T, heads * HEAD_DIM))
+    od = _f64(o, (T, heads * HEAD_DIM))
+    ld = _f64(lse, (heads, T))
+    dq = np.empty((heads, T, HEAD_DIM))
+    dk = np.empty((kv_heads, T, HEAD_DIM))
+    dvT = np.empty((kv_heads, HEAD_DIM, T))
+    D = np.empty((heads, T))
+    rc = lib.oracle_attn_bwd(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                             _ptr(vb, ctypes.c_uint16), _ptr(od, ctypes.c_double),
+                             _ptr(ld, ctypes.c_double), _ptr(gb, ctypes.c_uint16), T, heads,
+                             kv_heads, ctypes.c_float(c), ctypes.c_float(s),
+                             _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                             _ptr(dvT, ctypes.c_double), _ptr(D, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return dq, dk, dvT, D
+
+
+def attn_bwd_rows(q, k, vT, o, lse, dO, T: int, heads: int, kv_heads: int, c: float, s: float,
+                  q_heads, q_rows, kv_heads_idx, kv_rows, threads: int = 0, lib=None):
+    """Sampled rows of the backward: dQ at (q_heads[r], q_rows[r]) and dK, dV at
+    (kv_heads_idx[r], kv_rows[r]).  Returns (dQ [n_q][64], dK [n_kv][64], dV [n_kv][64])."""
+    lib = lib or _load()
+    qb = _bits(q, (heads, T, HEAD_DIM))
+    kb = _bits(k, (kv_heads, T, HEAD_DIM))
+    vb = _bits(vT, (kv_heads, HEAD_DIM, T))
+    gb = _bits(dO, (T, heads * HEAD_DIM))
+    od = _f64(o, (T, heads * HEAD_DIM))
+    ld = _f64(lse, (heads, T))
+    qh = np.ascontiguousarray(q_heads, dtype=np.int64)
+    qi = np.ascontiguousarray(q_rows, dtype=np.int64)
+    kg = np.ascontiguousarray(kv_heads_idx, dtype=np.int64)
+    kj = np.ascontiguousarray(kv_rows, dtype=np.int64)
+    if qh.shape != qi.shape or kg.shape != kj.shape:
+        raise ValueError("index arrays must pair up")
+    dq = np.empty((qh.shape[0], HEAD_DIM))
+    dk = np.empty((kg.shape[0], HEAD_DIM))
+    dv = np.empty((kg.shape[0], HEAD_DIM))
+    rc = lib.oracle_attn_bwd_rows(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                  _ptr(vb, ctypes.c_uint16), _ptr(od, ctypes.c_double),
+                                  _ptr(ld, ctypes.c_double), _ptr(gb, ctypes.c_uint16), T, heads,
+                                  kv_heads, ctypes.c_float(c), ctypes.c_float(s),
+                                  _ptr(qh, ctypes.c_int64), _ptr(qi, ctypes.c_int64), qh.shape[0],
+                                  _ptr(kg, ctypes.c_int64), _ptr(kj, ctypes.c_int64), kg.shape[0],
+                                  _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                  _ptr(dv, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape or an index")
+    return dq, dk, dv

@@ -26,6 +26,9 @@
  * the plain two-pass definition (no streaming, no tiling), so it shares no
  * algorithm with the GPU kernel.  The diagonal key j = i is kept (the page's
  * diagonal-tile mask removes only columns beyond the row).
+ *
+ * The backward pass of the same page (dQ, dK, dV from dO, the forward's O
+ * and L) is further below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -220,4 +223,191 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *vT,
     }
     (void)nt;
     return failed ? -1 : 0;
+}
+
+/*
+ * Backward pass, following the backward comment of the page
+ * "Realization/Nvidia/SM86/StreamingAttentionSM86.alpha": with the forward's
+ * base-2 log-sum-exp L and output O given,
+ *
+ *   P_ij  = 2^(c S_ij - L_i)          for keys j <= i   (S = Q K^T)
+ *   dP_ij = sum_e dO_ie V_je          (dP = dO V^T)
+ *   D_i   = sum_e dO_ie O_ie          (the row term)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = s sum_j dS_ij K_j,   dK_j = s sum_i dS_ij Q_i,   dV_j = sum_i P_ij dO_i
+ *
+ * with s the natural score scale; dK and dV are summed over the query heads
+ * of each K/V head's group (the page's grouped-gradient reduce).  O and L are
+ * taken as given (fp64 arrays), so the oracle follows the same inputs the
+ * kernels get.  Layouts: dO and O token-major [T][heads*64]; L and D
+ * [heads][T]; dQ [heads][T][64]; dK [kv_heads][T][64]; dV^T [kv_heads][64][T].
+ */
+static double dot64_hq(const uint16_t *a, const double *b)
+{
+    double s = 0.0;
+    for (int e = 0; e < HEAD_DIM; ++e)
+        s += g_half[a[e]] * b[e];
+    return s;
+}
+
+/* D for every (head, row): D[h][i] = sum_e dO[i][h*64+e] O[i][h*64+e]. */
+static void oracle_row_terms(const double *o, const uint16_t *dO, int64_t T, int64_t heads,
+                             double *D)
+{
+    for (int64_t h = 0; h < heads; ++h)
+        for (int64_t i = 0; i < T; ++i) {
+            const uint16_t *g = dO + (i * heads + h) * HEAD_DIM;
+            const double *oo = o + (i * heads + h) * HEAD_DIM;
+            double s = 0.0;
+            for (int e = 0; e < HEAD_DIM; ++e)
+                s += g_half[g[e]] * oo[e];
+            D[h * T + i] = s;
+        }
+}
+
+/* dQ row i of head h (D for all rows given). */
+static void oracle_dq_row(const uint16_t *q, const uint16_t *k, const uint16_t *vT,
+                          const double *lse, const uint16_t *dO, const double *D,
+                          int64_t T, int64_t heads, int64_t kv_heads, double c, double s,
+                          int64_t h, int64_t i, double *out)
+{
+    const int64_t g = h / (heads / kv_heads);
+    double qd[HEAD_DIM], gd[HEAD_DIM], acc[HEAD_DIM];
+    for (int e = 0; e < HEAD_DIM; ++e) {
+        qd[e] = g_half[q[(h * T + i) * HEAD_DIM + e]];
+        gd[e] = g_half[dO[(i * heads + h) * HEAD_DIM + e]];
+        acc[e] = 0.0;
+    }
+    for (int64_t j = 0; j <= i; ++j) {
+        const uint16_t *kj = k + (g * T + j) * HEAD_DIM;
+        const double p = exp2(c * dot64_hq(kj, qd) - lse[h * T + i]);
+        double dp = 0.0;
+        for (int e = 0; e < HEAD_DIM; ++e)
+            dp += gd[e] * g_half[vT[(g * HEAD_DIM + e) * T + j]];
+        const double ds = p * (dp - D[h * T + i]);
+        for (int e = 0; e < HEAD_DIM; ++e)
+            acc[e] += ds * g_half[kj[e]];
+    }
+    for (int e = 0; e < HEAD_DIM; ++e)
+        out[e] = s * acc[e];
+}
+
+/* dK and dV rows j of K/V head g, summed over the group's query heads. */
+static void oracle_dkv_row(const uint16_t *q, const uint16_t *k, const uint16_t *vT,
+                           const double *lse, const uint16_t *dO, const double *D,
+                           int64_t T, int64_t heads, int64_t kv_heads, double c, double s,
+                           int64_t g, int64_t j, double *dk_out, double *dv_out)
+{
+    const int64_t group = heads / kv_heads;
+    double kd[HEAD_DIM], vd[HEAD_DIM], dk[HEAD_DIM], dv[HEAD_DIM];
+    for (int e = 0; e < HEAD_DIM; ++e) {
+        kd[e] = g_half[k[(g * T + j) * HEAD_DIM + e]];
+        vd[e] = g_half[vT[(g * HEAD_DIM + e) * T + j]];
+        dk[e] = dv[e] = 0.0;
+    }
+    for (int64_t h = g * group; h < (g + 1) * group; ++h)
+        for (int64_t i = j; i < T; ++i) {
+            const uint16_t *qi = q + (h * T + i) * HEAD_DIM;
+            const uint16_t *gi = dO + (i * heads + h) * HEAD_DIM;
+            const double p = exp2(c * dot64_hq(qi, kd) - lse[h * T + i]);
+            const double dp = dot64_hq(gi, vd);
+            const double ds = p * (dp - D[h * T + i]);
+            for (int e = 0; e < HEAD_DIM; ++e) {
+                dk[e] += ds * g_half[qi[e]];
+                dv[e] += p * g_half[gi[e]];
+            }
+        }
+    for (int e = 0; e < HEAD_DIM; ++e) {
+        dk_out[e] = s * dk[e];
+        dv_out[e] = dv[e];
+    }
+}
+
+/*
+ * Full backward.  o: fp64 [T][heads*64]; lse: fp64 [heads][T]; dO: binary16
+ * [T][heads*64].  Writes dq [heads][T][64], dk [kv_heads][T][64],
+ * dvT [kv_heads][64][T] and D [heads][T].  Returns 0, or -1 on a bad shape.
+ */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *vT, const double *o,
+                    const double *lse, const uint16_t *dO, int64_t T, int64_t heads,
+                    int64_t kv_heads, float c, float s, double *dq, double *dk, double *dvT,
+                    double *D, int threads)
+{
+    if (check_shape(T, heads, kv_heads))
+        return -1;
+    half_table_init();
+    oracle_row_terms(o, dO, T, heads, D);
+    const double cd = (double)c, sd = (double)s;
+    const int nt = resolve_threads(threads);
+    (void)nt;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16) collapse(2) nowait
+#endif
+        for (int64_t h = 0; h < heads; ++h)
+            for (int64_t i = 0; i < T; ++i)
+                oracle_dq_row(q, k, vT, lse, dO, D, T, heads, kv_heads, cd, sd, h, i,
+                              dq + (h * T + i) * HEAD_DIM);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 16) collapse(2)
+#endif
+        for (int64_t g = 0; g < kv_heads; ++g)
+            for (int64_t j = 0; j < T; ++j) {
+                double dkr[HEAD_DIM], dvr[HEAD_DIM];
+                oracle_dkv_row(q, k, vT, lse, dO, D, T, heads, kv_heads, cd, sd, g, j, dkr, dvr);
+                for (int e = 0; e < HEAD_DIM; ++e) {
+                    dk[(g * T + j) * HEAD_DIM + e] = dkr[e];
+                    dvT[(g * HEAD_DIM + e) * T + j] = dvr[e];
+                }
+            }
+    }
+    return 0;
+}
+
+/*
+ * Sampled rows of the backward: n_q (head, row) pairs of dQ and n_kv
+ * (kv_head, row) pairs of dK and dV.  Needs the row terms of every row, so
+ * it computes D first (cheap: one dot product per row).  dq_out [n_q][64],
+ * dk_out and dv_out [n_kv][64].  Returns 0, or -1 on a bad shape or index.
+ */
+int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *vT,
+                         const double *o, const double *lse, const uint16_t *dO, int64_t T,
+                         int64_t heads, int64_t kv_heads, float c, float s,
+                         const int64_t *qh, const int64_t *qi, int64_t n_q,
+                         const int64_t *kg, const int64_t *kj, int64_t n_kv,
+                         double *dq_out, double *dk_out, double *dv_out, int threads)
+{
+    if (check_shape(T, heads, kv_heads))
+        return -1;
+    for (int64_t r = 0; r < n_q; ++r)
+        if (qh[r] < 0 || qh[r] >= heads || qi[r] < 0 || qi[r] >= T)
+            return -1;
+    for (int64_t r = 0; r < n_kv; ++r)
+        if (kg[r] < 0 || kg[r] >= kv_heads || kj[r] < 0 || kj[r] >= T)
+            return -1;
+    half_table_init();
+    double *D = (double *)malloc(sizeof(double) * (size_t)(heads * T));
+    if (!D)
+        return -1;
+    oracle_row_terms(o, dO, T, heads, D);
+    const double cd = (double)c, sd = (double)s;
+    const int nt = resolve_threads(threads);
+    (void)nt;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+    for (int64_t r = 0; r < n_q + n_kv; ++r) {
+        if (r < n_q)
+            oracle_dq_row(q, k, vT, lse, dO, D, T, heads, kv_heads, cd, sd, qh[r], qi[r],
+                          dq_out + r * HEAD_DIM);
+        else
+            oracle_dkv_row(q, k, vT, lse, dO, D, T, heads, kv_heads, cd, sd, kg[r - n_q],
+                           kj[r - n_q], dk_out + (r - n_q) * HEAD_DIM,
+                           dv_out + (r - n_q) * HEAD_DIM);
+    }
+    free(D);
+    return 0;
 }
