@@ -233,8 +233,8 @@ def test_rejects_bad_shapes():
 MUTANTS = {
     "natural_exp": ("t[j] = exp2(t[j] - m);", "t[j] = exp(t[j] - m);"),
     "natural_log": ("*lse = m + log2(l);", "*lse = m + log(l);"),
-    "no_diagonal": ("for (int64_t j = 0; j <= i; ++j) {\n        const uint16_t *kj",
-                    "for (int64_t j = 0; j < i; ++j) {\n        const uint16_t *kj"),
+    "no_diagonal": ("for (int64_t j = 0; j <= i; ++j) {\n        const uint16_t *kj = k + (g * T + j) * HEAD_DIM;\n        double s = 0.0;",
+                    "for (int64_t j = 0; j < i; ++j) {\n        const uint16_t *kj = k + (g * T + j) * HEAD_DIM;\n        double s = 0.0;"),
     "interleaved_groups": ("const int64_t g = h / group;", "const int64_t g = h % kv_heads;"),
     "v_not_transposed": ("acc += t[j] * g_half[ve[j]];",
                          "acc += t[j] * g_half[vT[(g * T + j) * HEAD_DIM + e]];"),
