@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the causal grouped-query attention forward pass.
+"""Seeded synthetic inputs for the causal grouped-query attention forward and
+backward passes.
 
 This module is shared by the CUDA path's tests and benchmark and by the oracle
 tests.  It draws random numbers and lays them out; it holds none of the
@@ -12,6 +13,9 @@ Recipe (identical for both sides, which then read the same binary16 buffers):
   * the workload's power-of-two scale factors applied in float32 (exact);
   * rounded to binary16 with round-to-nearest-even (numpy's cast);
   * V transposed per K/V head to V^T [kv_heads][64][T].
+For the backward pass the output gradient dO [T][heads*64] (O's token-major
+layout) is drawn from its own Philox stream, keyed by the seed plus
+0x9E3779B9, as standard-normal float32 rounded to binary16.
 The scale constant c is the binary32 value nearest 0.125 / ln 2 (the head
 width 64 gives the score scale 1/sqrt(64) = 0.125).
 """
@@ -97,3 +101,13 @@ def make_inputs(w: Workload):
     k16 = k.astype(np.float16)
     vT16 = np.ascontiguousarray(v.astype(np.float16).transpose(0, 2, 1))
     return q16, k16, vT16
+
+
+GRAD_SEED_OFFSET = 0x9E3779B9
+
+
+def make_output_grad(w: Workload):
+    """Returns dO [T][H*64] as a binary16 numpy array (the backward's input)."""
+    rng = np.random.Generator(np.random.Philox(w.seed + GRAD_SEED_OFFSET))
+    g = rng.standard_normal((w.T, w.heads * HEAD_DIM), dtype=np.float32)
+    return g.astype(np.float16)

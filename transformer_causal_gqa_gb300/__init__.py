@@ -1,15 +1,19 @@
-"""GB300 (sm_103a) causal grouped-query attention forward, streaming normalised sum.
+"""GB300 (sm_103a) causal grouped-query attention: the forward pass as a
+streaming normalised sum, and its backward pass.
 
-A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h``
-(``libattn_gb300.so``): it checks tensor dtypes, devices and contiguity, and
-passes raw pointers, sizes and the stream handle.  Every step of the forward
-pass runs in the library's CUDA kernel; there is no CPU path.  If the library
-has not been built, every entry point raises ``RuntimeError``.
+A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h`` and
+``include/attn_bwd.h`` (``libattn_gb300.so``): it checks tensor dtypes,
+devices and contiguity, and passes raw pointers, sizes and the stream handle.
+Every step of both passes runs in the library's CUDA kernels; there is no CPU
+path.  If the library has not been built, every entry point raises
+``RuntimeError``.
 
 Layouts (the page "Realization/Nvidia/SM86/StreamingAttentionSM86.alpha"):
 q binary16 [heads][T][64], k binary16 [kv_heads][T][64], vT binary16
-[kv_heads][64][T]; outputs o binary16 [T][heads*64] and lse binary32
-[heads][T] (base-2 log-sum-exp).
+[kv_heads][64][T]; forward outputs o binary16 [T][heads*64] and lse binary32
+[heads][T] (base-2 log-sum-exp).  Backward: dO binary16 [T][heads*64] (O's
+layout); outputs dq binary32 [heads][T][64], dk binary32 [kv_heads][T][64],
+dvT binary32 [kv_heads][64][T].
 """
 from __future__ import annotations
 
@@ -28,10 +32,11 @@ ATTN_ELAUNCH = -4
 ATTN_EDEVICE = -5
 ATTN_ETIMEOUT = -6
 
-# every symbol include/attn_fwd.h declares
+# every symbol include/attn_fwd.h and include/attn_bwd.h declare
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
-            "attn_status_string")
+            "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
+            "attn_bwd_last_device_status")
 
 _lib = None
 
@@ -71,6 +76,12 @@ def load_library():
     lib.attn_test_inject_stall.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, f, f, vp, sz, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = sz
+    lib.attn_bwd_last_device_status.argtypes = [vp]
+    lib.attn_bwd_last_device_status.restype = i
     _lib = lib
     return lib
 
@@ -178,3 +189,54 @@ def attention(q, k, vT, c: float, stream=None):
     lse = torch.empty((heads, T), dtype=torch.float32, device=q.device)
     attn_fwd(q, k, vT, o, lse, T, heads, kv_heads, c, stream)
     return o, lse
+
+
+def attn_bwd_workspace_bytes(T: int, heads: int, kv_heads: int) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(int(T), int(heads), int(kv_heads)))
+
+
+def attn_bwd(q, k, vT, o, lse, dO, dq, dk, dvT, T: int, heads: int, kv_heads: int, c: float,
+             s: float, workspace, stream=None) -> None:
+    """Backward pass on CUDA tensors, queued on ``stream`` (default: torch's current).
+    o and lse are the forward's outputs for q, k, vT and c; s is the natural score
+    scale.  ``workspace`` is a CUDA uint8 tensor of at least attn_bwd_workspace_bytes
+    bytes (256-byte aligned, as torch's allocations are)."""
+    import torch
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T))
+    _check_tensor("o", o, torch.float16, (T, heads * HEAD_DIM))
+    _check_tensor("lse", lse, torch.float32, (heads, T))
+    _check_tensor("dO", dO, torch.float16, (T, heads * HEAD_DIM))
+    _check_tensor("dq", dq, torch.float32, (heads, T, HEAD_DIM))
+    _check_tensor("dk", dk, torch.float32, (kv_heads, T, HEAD_DIM))
+    _check_tensor("dvT", dvT, torch.float32, (kv_heads, HEAD_DIM, T))
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace: must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().attn_bwd(q.data_ptr(), k.data_ptr(), vT.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dvT.data_ptr(), int(T), int(heads), int(kv_heads), float(c),
+                                 float(s), workspace.data_ptr(), nbytes, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+
+
+def bwd_last_device_status(stream=None) -> int:
+    """Synchronises ``stream``; ATTN_OK, or ATTN_ETIMEOUT if a backward kernel wait gave up."""
+    return int(load_library().attn_bwd_last_device_status(_stream_handle(stream)))
+
+
+def attention_backward(q, k, vT, o, lse, dO, c: float, s: float, stream=None):
+    """Allocates the gradients and the workspace with torch and runs attn_bwd;
+    returns (dq, dk, dvT)."""
+    import torch
+    heads, T, _ = q.shape
+    kv_heads = k.shape[0]
+    dq = torch.empty((heads, T, HEAD_DIM), dtype=torch.float32, device=q.device)
+    dk = torch.empty((kv_heads, T, HEAD_DIM), dtype=torch.float32, device=q.device)
+    dvT = torch.empty((kv_heads, HEAD_DIM, T), dtype=torch.float32, device=q.device)
+    ws = torch.empty(attn_bwd_workspace_bytes(T, heads, kv_heads), dtype=torch.uint8,
+                     device=q.device)
+    attn_bwd(q, k, vT, o, lse, dO, dq, dk, dvT, T, heads, kv_heads, c, s, ws, stream)
+    return dq, dk, dvT
