@@ -32,13 +32,13 @@
  *   dvT  binary32 [kv_heads][64][T]              -- output
  *
  * Ownership: the caller owns every buffer, including `workspace`, where the
- * call keeps transposed binary16 copies of V, K, Q and dO and the row terms D
- * between its launches.  The library allocates a 4-byte status word per
- * device on first use and never frees it; nothing is allocated per call.
+ * call keeps the row terms D (binary32 [heads][T]) between its two launches.
+ * The library allocates a 4-byte status word per device on first use and
+ * never frees it; nothing is allocated per call.
  *
  * Errors: every entry point returns an attn_status (attn_fwd.h).  Argument
- * errors are detected on the host before anything is launched.  The launches
- * (four transposes, the query kernel, the key kernel) are asynchronous and
+ * errors are detected on the host before anything is launched.  The two
+ * launches (the query kernel, then the key kernel) are asynchronous and
  * ordered on `stream`.
  */
 #ifndef ATTN_BWD_H
@@ -54,8 +54,8 @@ extern "C" {
 
 /*
  * attn_bwd_workspace_bytes -- device bytes attn_bwd needs as `workspace` for
- * the given shape (2 * (heads + kv_heads) * T * 64 * 2 + heads * T * 4, each
- * part rounded up to 256 bytes), or 0 if the shape is not admitted.
+ * the given shape (heads * T * 4, rounded up to 256 bytes), or 0 if the
+ * shape is not admitted.
  */
 size_t attn_bwd_workspace_bytes(int T, int heads, int kv_heads);
 

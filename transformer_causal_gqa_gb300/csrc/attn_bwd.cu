@@ -10,15 +10,15 @@
 // rounded to binary16 for their products; every sum stays binary32.
 //
 // GB300 realisation: two persistent warp-specialised kernels (one TMA warp,
-// tcgen05 MMA issuer warps, four compute warps with one thread per
-// tensor-memory lane).  The query launch makes D and dQ per (query head,
-// 128-row tile); the key launch makes dK and dV per (K/V head, 128-key tile)
-// and runs over every query head of the group in turn, so the group sum
-// happens in the tensor-memory accumulator instead of a separate reduce pass.
-// Products whose B operand would run along the wrong dimension read
-// transposed copies (V, K^T, Q^T, dO^T) that a transpose kernel writes into
-// the caller's workspace first, so every MMA operand is K-major.  Every wait
-// is bounded (1 s), as in the forward.
+// tcgen05 MMA issuer warps, eight compute warps, one tile row per thread and
+// half the tile's columns per warpgroup).  The query launch makes D and dQ
+// per (query head, 128-row tile); the key launch makes dK and dV per (K/V
+// head, 128-key tile) and runs over every query head of the group in turn, so
+// the group sum happens in the tensor-memory accumulator instead of a
+// separate reduce pass.  Operands are read where they lie: a product whose
+// operand runs along the other dimension (V^T for dP, K for dQ, Q and dO for
+// dK and dV) reads its tile MN-major, so nothing is transposed in memory.
+// Every wait is bounded (1 s), as in the forward.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -41,7 +41,6 @@ constexpr int kTile = 128;                        // query rows / keys per tile 
 constexpr uint32_t kTileBytes = kTile * kD * 2;   // one binary16 tile: 16 KiB
 constexpr uint32_t kHalfTileBytes = kTileBytes / 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kThreads = 256;                     // 8 warps
 constexpr uint32_t kTmemCols = 512;
 
 // ---------------------------------------------------------------------------- shared pieces
@@ -123,25 +122,31 @@ __device__ __forceinline__ int unit_of(int k, int units) {
 
 // ============================================================================ query launch
 // Unit = (query head h, 128-row query tile qt), latest (heaviest) tiles first;
-// key tiles 0 .. qt.  Tensor memory: S at 0, dP at 128 (fp32, 128 columns
-// each), dS at 256 (binary16 pairs, 64 columns), dQ at 320 (fp32, 64 columns).
+// key tiles 0 .. qt.  Eight compute warps: warp w serves tensor-memory lanes
+// 32 (w % 4) .. +31 (one query row per thread) and key columns 64 (w / 4) ..
+// +63 of each tile.  Tensor memory: S in two buffers at 0 and 128 (so S of
+// the next tile is formed while this one is processed), dP at 256 (fp32),
+// dS at 384 (binary16 pairs, 64 columns), dQ at 448 (fp32, 64 columns).
 namespace qlaunch {
-constexpr int kStages = 3;                       // ring of {K, V, K^T} tiles
-constexpr uint32_t kStageBytes = 3 * kTileBytes;
+constexpr int kStages = 4;                       // ring of {K tile, V^T tile}
+constexpr uint32_t kStageBytes = 2 * kTileBytes;
 constexpr uint32_t kOffQ = 0;                    // Q tile, dO tile
 constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarQFull = 0, kBarQEmpty = 1;
 constexpr int kBarKvFull = 2, kBarKvEmpty = 2 + kStages;
-constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 1;
-constexpr int kBarDsFull = kBarSFree + 1, kBarDqDone = kBarDsFull + 1;
+constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 2;   // two each
+constexpr int kBarDpFull = kBarSFree + 2, kBarDpFree = kBarDpFull + 1;
+constexpr int kBarDsFull = kBarDpFree + 1, kBarDqDone = kBarDsFull + 1;
 constexpr int kBarDrain = kBarDqDone + 1;        // + issuer warp (0, 1)
 constexpr int kNumBars = kBarDrain + 2;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320;
-constexpr int kWarpSdp = 4, kWarpDq = 5, kWarpLoad = 6;
+constexpr uint32_t kColS = 0, kColDP = 256, kColDS = 384, kColDQ = 448;
+constexpr int kComputeWarps = 8;
+constexpr int kWarpSdp = 8, kWarpDq = 9, kWarpLoad = 10;
+constexpr int kThreads = 32 * 11;
 
 struct Unit {
   int h, g, qt, nk;   // nk: key tiles 0 .. qt (the diagonal)
@@ -157,8 +162,8 @@ __device__ __forceinline__ Unit decode(int u, const BwdParams &p) {
 }
 
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const CUtensorMap *tmK,
-                          const CUtensorMap *tmV, const CUtensorMap *tmKT, const BwdParams &p,
-                          const Sync &sy, uint32_t smem) {
+                          const CUtensorMap *tmVT, const BwdParams &p, const Sync &sy,
+                          uint32_t smem) {
   const int units = p.heads * p.q_tiles;
   uint32_t pos = 0, pos_issued = 0, q_issued = 0;
   int k = 0;
@@ -177,9 +182,8 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const
       mbar_arrive_expect_tx(full, kStageBytes);
       pos_issued = pos + 1;
       tma_load_3d(dst, tmK, full, 0, j * kTile, w.g);
-      tma_load_3d(dst + kTileBytes, tmV, full, 0, j * kTile, w.g);
-      tma_load_3d(dst + 2 * kTileBytes, tmKT, full, j * kTile, 0, w.g);
-      tma_load_3d(dst + 2 * kTileBytes + kHalfTileBytes, tmKT, full, j * kTile + kTile / 2, 0, w.g);
+      tma_load_3d(dst + kTileBytes, tmVT, full, j * kTile, 0, w.g);
+      tma_load_3d(dst + kTileBytes + kHalfTileBytes, tmVT, full, j * kTile + kTile / 2, 0, w.g);
     }
   }
   return;
@@ -191,33 +195,36 @@ drain:
   if (q_issued > 0) sy.drain_wait(kBarQFull, (q_issued - 1) & 1);
 }
 
-// S = Q K^T and dP = dO V^T for every key tile, once the compute warps have
-// pulled the previous pair into registers.
+// S = Q K^T (both K-major) into the S buffer of the tile's parity, then
+// dP = dO V^T (B read MN-major from the V^T tile: 64-key halves 8 KiB apart).
 __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
-  constexpr uint32_t id = idesc_f16_f32(kTile, kTile);
+  constexpr uint32_t idS = idesc_f16_f32(kTile, kTile);
+  constexpr uint32_t idDP = idesc_f16_f32_mn(kTile, kTile, false, true);
   const int units = p.heads * p.q_tiles;
-  uint32_t pos = 0, issued = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
     if (!sy.wait_warp(kBarQFull, k & 1, 111)) goto drain;
     tc_fence_after();
     for (int j = 0; j < w.nk; ++j, ++pos) {
-      const uint32_t st = pos % kStages;
+      const uint32_t st = pos % kStages, b = pos & 1;
       if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 112)) goto drain;
-      if (!sy.wait_warp(kBarSFree, (issued & 1) ^ 1, 113)) goto drain;
-      ++issued;
+      if (!sy.wait_warp(kBarSFree + b, ((pos >> 1) & 1) ^ 1, 113)) goto drain;
       tc_fence_after();
       const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
-        mma_ss(tmem + kColS, sw128_desc(smem + kOffQ + e * 32), sw128_desc(kb + e * 32), id,
-               e > 0 ? 1u : 0u);
+        mma_ss(tmem + kColS + 128u * b, sw128_desc(smem + kOffQ + e * 32), sw128_desc(kb + e * 32),
+               idS, e > 0 ? 1u : 0u);
+      mma_commit(sy.bar(kBarSFull + b));
+      if (!sy.wait_warp(kBarDpFree, (pos & 1) ^ 1, 114)) goto drain;
+      tc_fence_after();
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
         mma_ss(tmem + kColDP, sw128_desc(smem + kOffQ + kTileBytes + e * 32),
-               sw128_desc(kb + kTileBytes + e * 32), id, e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarSFull));
+               sw128_mn_desc(kb + kTileBytes + e * 2048, kHalfTileBytes), idDP, e > 0 ? 1u : 0u);
+      mma_commit(sy.bar(kBarDpFull));
       mma_commit(sy.bar(kBarKvEmpty + st));
     }
     mma_commit(sy.bar(kBarQEmpty));
@@ -228,26 +235,24 @@ drain:
   sy.drain_wait(kBarDrain + 0, 0);
 }
 
-// dQ += dS K (A = dS from tensor memory, B = K^T, K-major over keys).
+// dQ += dS K (A = dS from tensor memory; B read MN-major from the K tile).
 __device__ void dq_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
-  constexpr uint32_t id = idesc_f16_f32(kTile, kD);
+  constexpr uint32_t id = idesc_f16_f32_mn(kTile, kD, false, true);
   const int units = p.heads * p.q_tiles;
-  uint32_t pos = 0, dphase = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarDsFull, dphase, 121)) goto drain;
-      dphase ^= 1;
+      if (!sy.wait_warp(kBarDsFull, pos & 1, 121)) goto drain;
       if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 122)) goto drain;
       tc_fence_after();
-      const uint32_t ktb = smem + kOffRing + st * kStageBytes + 2 * kTileBytes;
+      const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
       for (int e = 0; e < kTile / 16; ++e)
-        mma_ts(tmem + kColDQ, tmem + kColDS + 8u * e,
-               sw128_desc(ktb + (e >> 2) * kHalfTileBytes + (e & 3) * 32), id,
-               (j > 0 || e > 0) ? 1u : 0u);
+        mma_ts(tmem + kColDQ, tmem + kColDS + 8u * e, sw128_mn_desc(kb + e * 2048, kHalfTileBytes),
+               id, (j > 0 || e > 0) ? 1u : 0u);
       mma_commit(sy.bar(kBarDqDone));
       mma_commit(sy.bar(kBarKvEmpty + st));
     }
@@ -258,14 +263,16 @@ drain:
   sy.drain_wait(kBarDrain + 1, 0);
 }
 
-// Compute warps: thread r owns query row r of the tile (tensor-memory lane r).
 __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) {
-  const int r = threadIdx.x & 127;
+  const int warp = threadIdx.x >> 5;
+  const int r = 32 * (warp & 3) + (threadIdx.x & 31);   // tile row (tensor-memory lane)
+  const int half = warp >> 2;                            // key columns 64 half .. +63
+  const int col0 = 64 * half;
   const bool leader = (threadIdx.x & 31) == 0;
-  const uint32_t lane_base = (uint32_t)(threadIdx.x & 96) << 16;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const float c = p.c;
   const int units = p.heads * p.q_tiles;
-  uint32_t sphase = 0, dqphase = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
@@ -292,57 +299,61 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
       }
       D = acc0 + acc1;
       L = p.lse[(size_t)w.h * p.T + row];
-      p.D[(size_t)w.h * p.T + row] = D;
+      if (half == 0) p.D[(size_t)w.h * p.T + row] = D;
     }
     const float negL = -L;
-    for (int j = 0; j < w.nk; ++j) {
-      if (!sy.wait_warp(kBarSFull, sphase, 131)) return;
-      sphase ^= 1;
+    for (int j = 0; j < w.nk; ++j, ++pos) {
+      const uint32_t b = pos & 1;
+      if (!sy.wait_warp(kBarSFull + b, (pos >> 1) & 1, 131)) return;
       tc_fence_after();
-      uint32_t pk[64];   // dS row: columns 2m, 2m+1 in pk[m]
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_base + kColS + 32u * c4, sr);
-        tmem_ld_x32(tmem + lane_base + kColDP + 32u * c4, dr);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = 32 * c4 + 2 * i;
-          float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, negL));
-          float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, negL));
-          if (j == w.qt) {            // diagonal tile: keys after the row get P = 0
-            if (col > r) p0 = 0.f;
-            if (col + 1 > r) p1 = 0.f;
-          }
-          const float ds0 = p0 * (__uint_as_float(dr[2 * i]) - D);
-          const float ds1 = p1 * (__uint_as_float(dr[2 * i + 1]) - D);
-          pk[16 * c4 + i] = pack_half2(ds0, ds1);
-        }
-      }
-      // S and dP are in registers: the next pair may be computed over them
+      uint32_t sr[64];
+      tmem_ld_x64(tmem + lane_base + kColS + 128u * b + col0, sr);
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarSFree));
+      if (leader) mbar_arrive(sy.bar(kBarSFree + b));
+      // P = 2^(S c - L); on the diagonal tile keys after the row get P = 0
+      const int lim = (j == w.qt) ? r - col0 : 1 << 30;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float pr = ex2(fmaf(__uint_as_float(sr[i]), c, negL));
+        sr[i] = __float_as_uint(i <= lim ? pr : 0.f);
+      }
+      if (!sy.wait_warp(kBarDpFull, pos & 1, 132)) return;
+      tc_fence_after();
+      uint32_t pk[32];   // dS: key columns col0 + 2m, +1 in pk[m]
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t dr[32];
+        tmem_ld_x32(tmem + lane_base + kColDP + col0 + 32u * c2, dr);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float ds0 = __uint_as_float(sr[32 * c2 + 2 * i]) * (__uint_as_float(dr[2 * i]) - D);
+          const float ds1 =
+              __uint_as_float(sr[32 * c2 + 2 * i + 1]) * (__uint_as_float(dr[2 * i + 1]) - D);
+          pk[16 * c2 + i] = pack_half2(ds0, ds1);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarDpFree));
       if (j > 0) {   // dS(j-1) K must be complete before dS is overwritten
-        if (!sy.wait_warp(kBarDqDone, dqphase, 132)) return;
-        dqphase ^= 1;
+        if (!sy.wait_warp(kBarDqDone, (pos - 1) & 1, 133)) return;
         tc_fence_after();
       }
-      tmem_st_x64(tmem + lane_base + kColDS, pk);
+      tmem_st_x32(tmem + lane_base + kColDS + 32u * half, pk);
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarDsFull));
     }
-    // epilogue: dQ = s (sum) once the last product is done
-    if (!sy.wait_warp(kBarDqDone, dqphase, 133)) return;
-    dqphase ^= 1;
+    // epilogue: dQ = s (sum) once the last product is done; each half writes 32 columns
+    if (!sy.wait_warp(kBarDqDone, (pos - 1) & 1, 134)) return;
     tc_fence_after();
-    uint32_t qr[64];
-    tmem_ld_x64(tmem + lane_base + kColDQ, qr);
+    uint32_t qr[32];
+    tmem_ld_x32(tmem + lane_base + kColDQ + 32u * half, qr);
     if (valid) {
-      float4 *dst = reinterpret_cast<float4 *>(p.dq + ((size_t)w.h * p.T + row) * kD);
+      float4 *dst = reinterpret_cast<float4 *>(p.dq + ((size_t)w.h * p.T + row) * kD + 32 * half);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
+      for (int i = 0; i < 8; ++i)
         dst[i] = make_float4(__uint_as_float(qr[4 * i]) * p.s, __uint_as_float(qr[4 * i + 1]) * p.s,
                              __uint_as_float(qr[4 * i + 2]) * p.s, __uint_as_float(qr[4 * i + 3]) * p.s);
     }
@@ -352,8 +363,8 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
 
 __global__ void __launch_bounds__(kThreads, 1)
     query_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmKT, const BwdParams p) {
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVT,
+                 const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t smem = (raw + 1023u) & ~1023u;
@@ -370,9 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sy.bar(kBarKvFull + i), 1);
       mbar_init(sy.bar(kBarKvEmpty + i), 2);   // S/dP issuer and dQ issuer
     }
-    mbar_init(sy.bar(kBarSFull), 1);
-    mbar_init(sy.bar(kBarSFree), 4);
-    mbar_init(sy.bar(kBarDsFull), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sy.bar(kBarSFull + i), 1);
+      mbar_init(sy.bar(kBarSFree + i), kComputeWarps);
+    }
+    mbar_init(sy.bar(kBarDpFull), 1);
+    mbar_init(sy.bar(kBarDpFree), kComputeWarps);
+    mbar_init(sy.bar(kBarDsFull), kComputeWarps);
     mbar_init(sy.bar(kBarDqDone), 1);
     mbar_init(sy.bar(kBarDrain + 0), 1);
     mbar_init(sy.bar(kBarDrain + 1), 1);
@@ -387,14 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
-  if (warp < 4) {
+  if (warp < kComputeWarps) {
     compute_role(p, sy, tmem);
   } else if (warp == kWarpSdp) {
     sdp_role(p, sy, smem, tmem);
   } else if (warp == kWarpDq) {
     dq_role(p, sy, smem, tmem);
   } else if (warp == kWarpLoad) {
-    if (lane == 0) load_role(&tmQ, &tmDO, &tmK, &tmV, &tmKT, p, sy, smem);
+    if (lane == 0) load_role(&tmQ, &tmDO, &tmK, &tmVT, p, sy, smem);
     __syncwarp();
   }
   tc_fence_before();
@@ -410,28 +425,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Unit = (K/V head g, 128-key tile kt), earliest (heaviest) tiles first.  A
 // unit steps through every query head z of the group and, for each, the
 // query tiles kt .. q_tiles-1, accumulating dK and dV over all of them.
-// Tensor memory: S^T at 0, dP^T at 128 (fp32), P^T at 256, dS^T at 320
-// (binary16 pairs), dV at 384, dK at 448 (fp32).
+// Eight compute warps: warp w serves lanes 32 (w % 4) .. +31 (one key per
+// thread) and query columns 64 (w / 4) .. +63.  Tensor memory: S^T at 0,
+// dP^T at 128 (fp32), P^T at 256, dS^T at 320 (binary16 pairs), dV at 384,
+// dK at 448 (fp32).
 namespace klaunch {
-constexpr int kStages = 2;   // ring of {Q, dO, Q^T, dO^T tiles, L, D}
-constexpr uint32_t kStageBytes = 4 * kTileBytes + 2 * kTile * 4;
-constexpr uint32_t kOffK = 0;                    // K tile, V tile
+constexpr int kStages = 4;   // ring of {Q tile, dO tile, L, D}
+constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;   // L and D: 512 bytes each
+constexpr uint32_t kOffK = 0;                              // K tile, V^T tile
 constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarKvFull = 0, kBarKvEmpty = 1;
 constexpr int kBarQFull = 2, kBarQEmpty = 2 + kStages;
 constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 1;
-constexpr int kBarPFull = kBarSFree + 1, kBarDvDone = kBarPFull + 1, kBarDkDone = kBarDvDone + 1;
+constexpr int kBarDpFull = kBarSFree + 1, kBarDpFree = kBarDpFull + 1;
+constexpr int kBarPFull = kBarDpFree + 1, kBarDvDone = kBarPFull + 1, kBarDkDone = kBarDvDone + 1;
 constexpr int kBarDrain = kBarDkDone + 1;        // + issuer warp (0..2)
 constexpr int kNumBars = kBarDrain + 3;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDS = 320, kColDV = 384, kColDK = 448;
-constexpr int kWarpSdp = 4, kWarpDv = 5, kWarpDk = 6, kWarpLoad = 7;
+constexpr int kComputeWarps = 8;
+constexpr int kWarpSdp = 8, kWarpDv = 9, kWarpDk = 10, kWarpLoad = 11;
+constexpr int kThreads = 32 * 12;
 // offsets inside a stage
-constexpr uint32_t kSQ = 0, kSDO = kTileBytes, kSQT = 2 * kTileBytes, kSDOT = 3 * kTileBytes;
-constexpr uint32_t kSL = 4 * kTileBytes, kSDd = kSL + kTile * 4;
+constexpr uint32_t kSQ = 0, kSDO = kTileBytes, kSL = 2 * kTileBytes, kSDd = kSL + kTile * 4;
 
 struct Unit {
   int g, kt, nq, steps;   // query tiles kt .. kt + nq - 1 for each of the group's heads
@@ -452,9 +471,8 @@ __device__ __forceinline__ void step_of(const Unit &w, int i, const BwdParams &p
   qt = w.kt + (i - z * w.nq);
 }
 
-__device__ void load_role(const CUtensorMap *tmK, const CUtensorMap *tmV, const CUtensorMap *tmQ,
-                          const CUtensorMap *tmDO, const CUtensorMap *tmQT,
-                          const CUtensorMap *tmDOT, const BwdParams &p, const Sync &sy,
+__device__ void load_role(const CUtensorMap *tmK, const CUtensorMap *tmVT, const CUtensorMap *tmQ,
+                          const CUtensorMap *tmDO, const BwdParams &p, const Sync &sy,
                           uint32_t smem) {
   const int units = p.kv_heads * p.q_tiles;
   uint32_t pos = 0, pos_issued = 0, kv_issued = 0;
@@ -465,7 +483,9 @@ __device__ void load_role(const CUtensorMap *tmK, const CUtensorMap *tmV, const 
     ++kv_issued;
     mbar_arrive_expect_tx(sy.bar(kBarKvFull), 2 * kTileBytes);
     tma_load_3d(smem + kOffK, tmK, sy.bar(kBarKvFull), 0, w.kt * kTile, w.g);
-    tma_load_3d(smem + kOffK + kTileBytes, tmV, sy.bar(kBarKvFull), 0, w.kt * kTile, w.g);
+    tma_load_3d(smem + kOffK + kTileBytes, tmVT, sy.bar(kBarKvFull), w.kt * kTile, 0, w.g);
+    tma_load_3d(smem + kOffK + kTileBytes + kHalfTileBytes, tmVT, sy.bar(kBarKvFull),
+                w.kt * kTile + kTile / 2, 0, w.g);
     for (int i = 0; i < w.steps; ++i, ++pos) {
       int h, qt;
       step_of(w, i, p, h, qt);
@@ -474,14 +494,10 @@ __device__ void load_role(const CUtensorMap *tmK, const CUtensorMap *tmV, const 
       const uint32_t dst = smem + kOffRing + st * kStageBytes;
       const uint32_t full = sy.bar(kBarQFull + st);
       const int rows = min(kTile, p.T - qt * kTile);      // query rows that exist (64 or 128)
-      mbar_arrive_expect_tx(full, 4 * kTileBytes + 2 * rows * 4);
+      mbar_arrive_expect_tx(full, 2 * kTileBytes + 2 * rows * 4);
       pos_issued = pos + 1;
       tma_load_3d(dst + kSQ, tmQ, full, 0, qt * kTile, h);
       tma_load_3d(dst + kSDO, tmDO, full, h * kD, qt * kTile, 0);
-      tma_load_3d(dst + kSQT, tmQT, full, qt * kTile, 0, h);
-      tma_load_3d(dst + kSQT + kHalfTileBytes, tmQT, full, qt * kTile + kTile / 2, 0, h);
-      tma_load_3d(dst + kSDOT, tmDOT, full, qt * kTile, 0, h);
-      tma_load_3d(dst + kSDOT + kHalfTileBytes, tmDOT, full, qt * kTile + kTile / 2, 0, h);
       bulk_load(dst + kSL, p.lse + (size_t)h * p.T + qt * kTile, rows * 4, full);
       bulk_load(dst + kSDd, p.D + (size_t)h * p.T + qt * kTile, rows * 4, full);
     }
@@ -495,11 +511,12 @@ drain:
   if (kv_issued > 0) sy.drain_wait(kBarKvFull, (kv_issued - 1) & 1);
 }
 
-// S^T = K Q^T and dP^T = V dO^T per step.
+// S^T = K Q^T (both K-major) and dP^T = V dO^T (A read MN-major from the V^T tile).
 __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
-  constexpr uint32_t id = idesc_f16_f32(kTile, kTile);
+  constexpr uint32_t idS = idesc_f16_f32(kTile, kTile);
+  constexpr uint32_t idDP = idesc_f16_f32_mn(kTile, kTile, true, false);
   const int units = p.kv_heads * p.q_tiles;
-  uint32_t pos = 0, issued = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
@@ -508,19 +525,21 @@ __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint
     for (int i = 0; i < w.steps; ++i, ++pos) {
       const uint32_t st = pos % kStages;
       if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 212)) goto drain;
-      if (!sy.wait_warp(kBarSFree, (issued & 1) ^ 1, 213)) goto drain;
-      ++issued;
+      if (!sy.wait_warp(kBarSFree, (pos & 1) ^ 1, 213)) goto drain;
       tc_fence_after();
       const uint32_t sb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
-        mma_ss(tmem + kColS, sw128_desc(smem + kOffK + e * 32), sw128_desc(sb + kSQ + e * 32), id,
+        mma_ss(tmem + kColS, sw128_desc(smem + kOffK + e * 32), sw128_desc(sb + kSQ + e * 32), idS,
                e > 0 ? 1u : 0u);
+      mma_commit(sy.bar(kBarSFull));
+      if (!sy.wait_warp(kBarDpFree, (pos & 1) ^ 1, 214)) goto drain;
+      tc_fence_after();
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
-        mma_ss(tmem + kColDP, sw128_desc(smem + kOffK + kTileBytes + e * 32),
-               sw128_desc(sb + kSDO + e * 32), id, e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarSFull));
+        mma_ss(tmem + kColDP, sw128_mn_desc(smem + kOffK + kTileBytes + e * 2048, kHalfTileBytes),
+               sw128_desc(sb + kSDO + e * 32), idDP, e > 0 ? 1u : 0u);
+      mma_commit(sy.bar(kBarDpFull));
       mma_commit(sy.bar(kBarQEmpty + st));
     }
     mma_commit(sy.bar(kBarKvEmpty));
@@ -531,31 +550,30 @@ drain:
   sy.drain_wait(kBarDrain + 0, 0);
 }
 
-// dV += P^T dO (B = dO^T) when which == 0, dK += dS^T Q (B = Q^T) when which == 1.
+// dV += P^T dO (B = dO tile) when which == 0, dK += dS^T Q (B = Q tile) when
+// which == 1; B is read MN-major from the tile.
 __device__ void acc_role(int which, const BwdParams &p, const Sync &sy, uint32_t smem,
                          uint32_t tmem) {
-  constexpr uint32_t id = idesc_f16_f32(kTile, kD);
+  constexpr uint32_t id = idesc_f16_f32_mn(kTile, kD, false, true);
   const int units = p.kv_heads * p.q_tiles;
   const uint32_t a_col = which ? kColDS : kColP;
   const uint32_t d_col = which ? kColDK : kColDV;
-  const uint32_t b_off = which ? kSQT : kSDOT;
+  const uint32_t b_off = which ? kSQ : kSDO;
   const int done_bar = which ? kBarDkDone : kBarDvDone;
-  uint32_t pos = 0, pphase = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
     for (int i = 0; i < w.steps; ++i, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarPFull, pphase, 221 + which)) goto drain;
-      pphase ^= 1;
+      if (!sy.wait_warp(kBarPFull, pos & 1, 221 + which)) goto drain;
       if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 223 + which)) goto drain;
       tc_fence_after();
       const uint32_t bb = smem + kOffRing + st * kStageBytes + b_off;
 #pragma unroll
       for (int e = 0; e < kTile / 16; ++e)
-        mma_ts(tmem + d_col, tmem + a_col + 8u * e,
-               sw128_desc(bb + (e >> 2) * kHalfTileBytes + (e & 3) * 32), id,
-               (i > 0 || e > 0) ? 1u : 0u);
+        mma_ts(tmem + d_col, tmem + a_col + 8u * e, sw128_mn_desc(bb + e * 2048, kHalfTileBytes),
+               id, (i > 0 || e > 0) ? 1u : 0u);
       mma_commit(sy.bar(done_bar));
       mma_commit(sy.bar(kBarQEmpty + st));
     }
@@ -566,16 +584,17 @@ drain:
   sy.drain_wait(kBarDrain + 1 + which, 0);
 }
 
-// Compute warps: thread r owns key row r of the tile (tensor-memory lane r);
-// columns are the step's 128 queries, whose L and D come from shared memory.
 __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *smem_gen,
                              uint32_t tmem) {
-  const int r = threadIdx.x & 127;
+  const int warp = threadIdx.x >> 5;
+  const int r = 32 * (warp & 3) + (threadIdx.x & 31);   // key row of the tile (lane)
+  const int half = warp >> 2;                            // query columns 64 half .. +63
+  const int col0 = 64 * half;
   const bool leader = (threadIdx.x & 31) == 0;
-  const uint32_t lane_base = (uint32_t)(threadIdx.x & 96) << 16;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const float c = p.c;
   const int units = p.kv_heads * p.q_tiles;
-  uint32_t pos = 0, sphase = 0, dvphase = 0, dkphase = 0;
+  uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
@@ -587,81 +606,87 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       // the stage's copies (L and D among them) are visible to this thread once it
       // has seen the stage's barrier complete
       if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 230)) return;
-      if (!sy.wait_warp(kBarSFull, sphase, 231)) return;
-      sphase ^= 1;
+      if (!sy.wait_warp(kBarSFull, pos & 1, 231)) return;
       tc_fence_after();
-      const float *Ls = reinterpret_cast<const float *>(smem_gen + kOffRing + st * kStageBytes + kSL);
-      const float *Ds = reinterpret_cast<const float *>(smem_gen + kOffRing + st * kStageBytes + kSDd);
-      const int first = qt * kTile - key;                // query index of column 0, minus the key
-      const int qlimit = min(kTile, p.T - qt * kTile);   // columns that are real queries
-      uint32_t pp[64], pd[64];   // P^T and dS^T rows: columns 2m, 2m+1 in [m]
+      uint32_t sr[64];
+      tmem_ld_x64(tmem + lane_base + kColS + col0, sr);
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarSFree));
+      const float *Ls =
+          reinterpret_cast<const float *>(smem_gen + kOffRing + st * kStageBytes + kSL) + col0;
+      const float *Ds =
+          reinterpret_cast<const float *>(smem_gen + kOffRing + st * kStageBytes + kSDd) + col0;
+      // column t is query qt*128 + col0 + t: it sees this key when it is not earlier,
+      // and exists when it is before the sequence end (the L, D of others are stale)
+      const int lo = key - (qt * kTile + col0);
+      const int hi = min(kTile, p.T - qt * kTile) - col0;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_base + kColS + 32u * c4, sr);
-        tmem_ld_x32(tmem + lane_base + kColDP + 32u * c4, dr);
+      for (int t4 = 0; t4 < 16; ++t4) {
+        const float4 L4 = *reinterpret_cast<const float4 *>(Ls + 4 * t4);
+        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const int col = 32 * c4 + 4 * i4;
-          const float4 L4 = *reinterpret_cast<const float4 *>(Ls + col);
-          const float4 D4 = *reinterpret_cast<const float4 *>(Ds + col);
-          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * t4 + e;
+          const float pr = ex2(fmaf(__uint_as_float(sr[t]), c, -Lv[e]));
+          sr[t] = __float_as_uint((t >= lo && t < hi) ? pr : 0.f);
+        }
+      }
+      if (!sy.wait_warp(kBarDpFull, pos & 1, 232)) return;
+      tc_fence_after();
+      uint32_t pp[32], pd[32];   // P^T and dS^T: query columns col0 + 2m, +1 in [m]
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t dr[32];
+        tmem_ld_x32(tmem + lane_base + kColDP + col0 + 32u * c2, dr);
+#pragma unroll
+        for (int t4 = 0; t4 < 8; ++t4) {
+          const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 32 * c2 + 4 * t4);
+          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
           float pv[4], dv[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            // causal: query (qt*128 + col + t) sees this key when it is not earlier;
-            // columns past the sequence end are not queries (their L, D are stale)
-            const bool live = (first + col + t >= 0) && (col + t < qlimit);
-            const float pr = ex2(fmaf(__uint_as_float(sr[4 * i4 + t]), c, -Lv[t]));
-            pv[t] = live ? pr : 0.f;
-            dv[t] = live ? pr * (__uint_as_float(dr[4 * i4 + t]) - Dv[t]) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            pv[e] = __uint_as_float(sr[32 * c2 + 4 * t4 + e]);
+            // a masked column has P = 0; its dP and D may be anything finite or not
+            dv[e] = pv[e] != 0.f ? pv[e] * (__uint_as_float(dr[4 * t4 + e]) - Dv[e]) : 0.f;
           }
-          pp[16 * c4 + 2 * i4] = pack_half2(pv[0], pv[1]);
-          pp[16 * c4 + 2 * i4 + 1] = pack_half2(pv[2], pv[3]);
-          pd[16 * c4 + 2 * i4] = pack_half2(dv[0], dv[1]);
-          pd[16 * c4 + 2 * i4 + 1] = pack_half2(dv[2], dv[3]);
+          pp[16 * c2 + 2 * t4] = pack_half2(pv[0], pv[1]);
+          pp[16 * c2 + 2 * t4 + 1] = pack_half2(pv[2], pv[3]);
+          pd[16 * c2 + 2 * t4] = pack_half2(dv[0], dv[1]);
+          pd[16 * c2 + 2 * t4 + 1] = pack_half2(dv[2], dv[3]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarSFree));
+      if (leader) mbar_arrive(sy.bar(kBarDpFree));
       if (i > 0) {   // the previous step's products must be done before P^T, dS^T are overwritten
-        if (!sy.wait_warp(kBarDvDone, dvphase, 232)) return;
-        dvphase ^= 1;
-        if (!sy.wait_warp(kBarDkDone, dkphase, 233)) return;
-        dkphase ^= 1;
+        if (!sy.wait_warp(kBarDvDone, (pos - 1) & 1, 233)) return;
+        if (!sy.wait_warp(kBarDkDone, (pos - 1) & 1, 234)) return;
         tc_fence_after();
       }
-      tmem_st_x64(tmem + lane_base + kColP, pp);
-      tmem_st_x64(tmem + lane_base + kColDS, pd);
+      tmem_st_x32(tmem + lane_base + kColP + 32u * half, pp);
+      tmem_st_x32(tmem + lane_base + kColDS + 32u * half, pd);
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarPFull));
     }
-    // epilogue: dV^T and s dK for this key row
-    if (!sy.wait_warp(kBarDvDone, dvphase, 234)) return;
-    dvphase ^= 1;
-    if (!sy.wait_warp(kBarDkDone, dkphase, 235)) return;
-    dkphase ^= 1;
+    // epilogue: the first half writes dV^T, the second s dK, for this key row
+    if (!sy.wait_warp(kBarDvDone, (pos - 1) & 1, 235)) return;
+    if (!sy.wait_warp(kBarDkDone, (pos - 1) & 1, 236)) return;
     tc_fence_after();
-    {
-      uint32_t vr[64];
-      tmem_ld_x64(tmem + lane_base + kColDV, vr);
-      if (key < p.T) {
+    uint32_t ar[64];
+    tmem_ld_x64(tmem + lane_base + (half ? kColDK : kColDV), ar);
+    if (key < p.T) {
+      if (half == 0) {
         float *dvt = p.dvT + (size_t)w.g * kD * p.T + key;
 #pragma unroll
-        for (int e = 0; e < kD; ++e) dvt[(size_t)e * p.T] = __uint_as_float(vr[e]);
-      }
-    }
-    {
-      uint32_t kr[64];
-      tmem_ld_x64(tmem + lane_base + kColDK, kr);
-      if (key < p.T) {
+        for (int e = 0; e < kD; ++e) dvt[(size_t)e * p.T] = __uint_as_float(ar[e]);
+      } else {
         float4 *dk = reinterpret_cast<float4 *>(p.dk + ((size_t)w.g * p.T + key) * kD);
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          dk[e] = make_float4(__uint_as_float(kr[4 * e]) * p.s, __uint_as_float(kr[4 * e + 1]) * p.s,
-                              __uint_as_float(kr[4 * e + 2]) * p.s, __uint_as_float(kr[4 * e + 3]) * p.s);
+          dk[e] = make_float4(__uint_as_float(ar[4 * e]) * p.s, __uint_as_float(ar[4 * e + 1]) * p.s,
+                              __uint_as_float(ar[4 * e + 2]) * p.s, __uint_as_float(ar[4 * e + 3]) * p.s);
       }
     }
     tc_fence_before();
@@ -669,9 +694,8 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    key_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    key_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVT,
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmQT, const __grid_constant__ CUtensorMap tmDOT,
                const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -690,8 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sy.bar(kBarQEmpty + i), 3);   // S^T/dP^T, dV and dK issuers
     }
     mbar_init(sy.bar(kBarSFull), 1);
-    mbar_init(sy.bar(kBarSFree), 4);
-    mbar_init(sy.bar(kBarPFull), 4);
+    mbar_init(sy.bar(kBarSFree), kComputeWarps);
+    mbar_init(sy.bar(kBarDpFull), 1);
+    mbar_init(sy.bar(kBarDpFree), kComputeWarps);
+    mbar_init(sy.bar(kBarPFull), kComputeWarps);
     mbar_init(sy.bar(kBarDvDone), 1);
     mbar_init(sy.bar(kBarDkDone), 1);
     for (int i = 0; i < 3; ++i) mbar_init(sy.bar(kBarDrain + i), 1);
@@ -706,14 +732,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
-  if (warp < 4) {
+  if (warp < kComputeWarps) {
     compute_role(p, sy, smem_gen, tmem);
   } else if (warp == kWarpSdp) {
     sdp_role(p, sy, smem, tmem);
   } else if (warp == kWarpDv || warp == kWarpDk) {
     acc_role(warp - kWarpDv, p, sy, smem, tmem);
   } else if (warp == kWarpLoad) {
-    if (lane == 0) load_role(&tmK, &tmV, &tmQ, &tmDO, &tmQT, &tmDOT, p, sy, smem);
+    if (lane == 0) load_role(&tmK, &tmVT, &tmQ, &tmDO, p, sy, smem);
     __syncwarp();
   }
   tc_fence_before();
@@ -724,29 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 }  // namespace klaunch
-
-// ============================================================================ transposes
-// dst[b][col][row] = src[b][row][col] for a batch of binary16 matrices whose
-// rows and columns are multiples of 64, through 64 x 64 shared-memory tiles.
-__global__ void __launch_bounds__(256) transpose_kernel(const __half *src, __half *dst, int rows,
-                                                        int cols, long long src_ld,
-                                                        long long src_batch, long long dst_ld,
-                                                        long long dst_batch) {
-  __shared__ __half tile[64][66];
-  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64, b = blockIdx.z;
-  if (c0 + 64 > cols || r0 + 64 > rows) return;
-  const __half *s = src + b * src_batch;
-  __half *d = dst + b * dst_batch;
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int rr = i >> 6, cc = i & 63;
-    tile[rr][cc] = s[(long long)(r0 + rr) * src_ld + c0 + cc];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int cc = i >> 6, rr = i & 63;
-    d[(long long)(c0 + cc) * dst_ld + r0 + rr] = tile[rr][cc];
-  }
-}
 
 // ============================================================================ host side
 struct BwdState {
@@ -807,22 +810,9 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
 
 size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// Workspace layout: V, K^T (per K/V head), Q^T, dO^T (per query head), all
-// binary16, then D (binary32 [heads][T]); each part starts on 256 bytes.
-struct BwdWorkspace {
-  size_t v, kt, qt, dot, d, total;
-};
-BwdWorkspace bwd_layout(int T, int heads, int kv_heads) {
-  BwdWorkspace w;
-  const size_t kvb = (size_t)kv_heads * T * kD * 2, hb = (size_t)heads * T * kD * 2;
-  w.v = 0;
-  w.kt = w.v + up256(kvb);
-  w.qt = w.kt + up256(kvb);
-  w.dot = w.qt + up256(hb);
-  w.d = w.dot + up256(hb);
-  w.total = w.d + up256((size_t)heads * T * 4);
-  return w;
-}
+// Workspace: the row terms D (binary32 [heads][T]) the query launch writes
+// for the key launch.
+size_t bwd_workspace(int T, int heads) { return up256((size_t)heads * T * 4); }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -843,7 +833,7 @@ int check_bwd_shape(int T, int heads, int kv_heads, float c, float s) {
 
 extern "C" size_t attn_bwd_workspace_bytes(int T, int heads, int kv_heads) {
   if (check_bwd_shape(T, heads, kv_heads, 1.f, 1.f)) return 0;
-  return bwd_layout(T, heads, kv_heads).total;
+  return bwd_workspace(T, heads);
 }
 
 extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void *o,
@@ -863,11 +853,11 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   for (const void *ptr : outs)
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return ATTN_EALIGN;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_EALIGN;
-  const BwdWorkspace ws = bwd_layout(T, heads, kv_heads);
-  if (workspace_bytes < ws.total) return ATTN_EINVAL;
+  const size_t ws_bytes = bwd_workspace(T, heads);
+  if (workspace_bytes < ws_bytes) return ATTN_EINVAL;
   const size_t hq = (size_t)heads * T * kD, kvn = (size_t)kv_heads * T * kD;
   const size_t in_sizes[] = {hq * 2, kvn * 2, kvn * 2, hq * 2, (size_t)heads * T * 4, hq * 2};
-  const size_t out_sizes[] = {hq * 4, kvn * 4, kvn * 4, ws.total};
+  const size_t out_sizes[] = {hq * 4, kvn * 4, kvn * 4, ws_bytes};
   for (int a = 0; a < 4; ++a) {
     for (int b = 0; b < 6; ++b)
       if (ranges_overlap(outs[a], out_sizes[a], ins[b], in_sizes[b])) return ATTN_EOVERLAP;
@@ -877,34 +867,11 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   BwdState *st = nullptr;
   if ((rc = bwd_state(&st))) return rc;
 
-  uint8_t *wsb = static_cast<uint8_t *>(workspace);
-  __half *Vh = reinterpret_cast<__half *>(wsb + ws.v);
-  __half *KTh = reinterpret_cast<__half *>(wsb + ws.kt);
-  __half *QTh = reinterpret_cast<__half *>(wsb + ws.qt);
-  __half *DOTh = reinterpret_cast<__half *>(wsb + ws.dot);
-  float *Dw = reinterpret_cast<float *>(wsb + ws.d);
-
-  // transposed copies, so every MMA operand is K-major
-  const dim3 tb(256);
-  transpose_kernel<<<dim3(T / 64, 1, kv_heads), tb, 0, stream>>>(
-      static_cast<const __half *>(vT), Vh, kD, T, T, (long long)kD * T, kD, (long long)T * kD);
-  transpose_kernel<<<dim3(1, T / 64, kv_heads), tb, 0, stream>>>(
-      static_cast<const __half *>(k), KTh, T, kD, kD, (long long)T * kD, T, (long long)kD * T);
-  transpose_kernel<<<dim3(1, T / 64, heads), tb, 0, stream>>>(
-      static_cast<const __half *>(q), QTh, T, kD, kD, (long long)T * kD, T, (long long)kD * T);
-  transpose_kernel<<<dim3(1, T / 64, heads), tb, 0, stream>>>(
-      static_cast<const __half *>(dO), DOTh, T, kD, (long long)heads * kD, kD, T,
-      (long long)kD * T);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-
   const uint64_t rowb = kD * 2, trow = (uint64_t)T * 2;
-  CUtensorMap tmQ, tmK, tmV, tmKT, tmQT, tmDOT, tmDO;
+  CUtensorMap tmQ, tmK, tmVT, tmDO;
   if (!encode_3d(&tmQ, q, kD, T, heads, rowb, rowb * T, kD, kTile) ||
       !encode_3d(&tmK, k, kD, T, kv_heads, rowb, rowb * T, kD, kTile) ||
-      !encode_3d(&tmV, Vh, kD, T, kv_heads, rowb, rowb * T, kD, kTile) ||
-      !encode_3d(&tmKT, KTh, T, kD, kv_heads, trow, trow * kD, kTile / 2, kD) ||
-      !encode_3d(&tmQT, QTh, T, kD, heads, trow, trow * kD, kTile / 2, kD) ||
-      !encode_3d(&tmDOT, DOTh, T, kD, heads, trow, trow * kD, kTile / 2, kD) ||
+      !encode_3d(&tmVT, vT, T, kD, kv_heads, trow, trow * kD, kTile / 2, kD) ||
       !encode_3d(&tmDO, dO, (uint64_t)heads * kD, T, 1, (uint64_t)heads * kD * 2,
                  (uint64_t)heads * kD * 2 * T, kD, kTile))
     return ATTN_ELAUNCH;
@@ -920,16 +887,16 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   p.lse = lse;
   p.o = static_cast<const __half *>(o);
   p.dO = static_cast<const __half *>(dO);
-  p.D = Dw;
+  p.D = static_cast<float *>(workspace);
   p.dq = dq;
   p.dk = dk;
   p.dvT = dvT;
   p.status = st->status;
   const int qunits = heads * p.q_tiles, kunits = kv_heads * p.q_tiles;
-  qlaunch::query_kernel<<<qunits < st->sms ? qunits : st->sms, kThreads, qlaunch::kSmemBytes,
-                          stream>>>(tmQ, tmDO, tmK, tmV, tmKT, p);
-  klaunch::key_kernel<<<kunits < st->sms ? kunits : st->sms, kThreads, klaunch::kSmemBytes,
-                        stream>>>(tmK, tmV, tmQ, tmDO, tmQT, tmDOT, p);
+  qlaunch::query_kernel<<<qunits < st->sms ? qunits : st->sms, qlaunch::kThreads,
+                          qlaunch::kSmemBytes, stream>>>(tmQ, tmDO, tmK, tmVT, p);
+  klaunch::key_kernel<<<kunits < st->sms ? kunits : st->sms, klaunch::kThreads,
+                        klaunch::kSmemBytes, stream>>>(tmK, tmVT, tmQ, tmDO, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }

@@ -146,12 +146,28 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared-memory matrix descriptor for an MN-major tile written by TMA with
+// 128-byte swizzle: each 128-byte row holds 64 consecutive M (or N) elements
+// for one K index, so consecutive K indices are 128 bytes apart.
+//   bits 16-29  leading-dimension byte offset >> 4: distance between
+//               successive 64-element blocks along M (or N)
+//   bits 32-45  stride byte offset >> 4: 1024 bytes between 8-row K groups
+// Advancing the start by 2048 bytes steps K by 16.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t smem_addr, uint32_t mn_block_bytes) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor, kind::f16: binary16 A and B, binary32 D, both
 // K-major, shape M x N.
 //   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
-//   15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
+//   15/16 A/B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with A and/or B MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32_mn(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f16_f32(M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane, then wait::ld.
