@@ -312,11 +312,16 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarSFree + b));
       // P = 2^(S c - L); on the diagonal tile keys after the row get P = 0
-      const int lim = (j == w.qt) ? r - col0 : 1 << 30;
+      if (j == w.qt) {
+        const int lim = r - col0;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float pr = ex2(fmaf(__uint_as_float(sr[i]), c, negL));
-        sr[i] = __float_as_uint(i <= lim ? pr : 0.f);
+        for (int i = 0; i < 64; ++i) {
+          const float pr = ex2(fmaf(__uint_as_float(sr[i]), c, negL));
+          sr[i] = __float_as_uint(i <= lim ? pr : 0.f);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sr[i] = __float_as_uint(ex2(fmaf(__uint_as_float(sr[i]), c, negL)));
       }
       if (!sy.wait_warp(kBarDpFull, pos & 1, 132)) return;
       tc_fence_after();
@@ -584,6 +589,55 @@ drain:
   sy.drain_wait(kBarDrain + 1 + which, 0);
 }
 
+// P^T = 2^(S^T c - L) over the thread's 64 query columns (in place).  With
+// kMasked, column t is kept only when lo <= t < hi: the query is not earlier
+// than the key and exists (columns past the sequence end carry stale L, D).
+template <bool kMasked>
+__device__ __forceinline__ void key_probs(uint32_t (&sr)[64], const float *Ls, float c, int lo,
+                                          int hi) {
+#pragma unroll
+  for (int t4 = 0; t4 < 16; ++t4) {
+    const float4 L4 = *reinterpret_cast<const float4 *>(Ls + 4 * t4);
+    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * t4 + e;
+      const float pr = ex2(fmaf(__uint_as_float(sr[t]), c, -Lv[e]));
+      sr[t] = __float_as_uint(!kMasked || (t >= lo && t < hi) ? pr : 0.f);
+    }
+  }
+}
+
+// dS^T = P^T (dP^T - D), with P^T and dS^T packed to binary16 pairs: query
+// columns 2m, 2m+1 of the thread's half in [m].  With kMasked a column whose
+// P is 0 gets dS = 0 whatever its dP and D hold.
+template <bool kMasked>
+__device__ __forceinline__ void key_grads(const uint32_t (&sr)[64], const float *Ds,
+                                          uint32_t dp_taddr, uint32_t (&pp)[32],
+                                          uint32_t (&pd)[32]) {
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t dr[32];
+    tmem_ld_x32(dp_taddr + 32u * c2, dr);
+#pragma unroll
+    for (int t4 = 0; t4 < 8; ++t4) {
+      const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 32 * c2 + 4 * t4);
+      const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+      float pv[4], dv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[e] = __uint_as_float(sr[32 * c2 + 4 * t4 + e]);
+        const float g = pv[e] * (__uint_as_float(dr[4 * t4 + e]) - Dv[e]);
+        dv[e] = !kMasked || pv[e] != 0.f ? g : 0.f;
+      }
+      pp[16 * c2 + 2 * t4] = pack_half2(pv[0], pv[1]);
+      pp[16 * c2 + 2 * t4 + 1] = pack_half2(pv[2], pv[3]);
+      pd[16 * c2 + 2 * t4] = pack_half2(dv[0], dv[1]);
+      pd[16 * c2 + 2 * t4 + 1] = pack_half2(dv[2], dv[3]);
+    }
+  }
+}
+
 __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *smem_gen,
                              uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
@@ -618,44 +672,22 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       const float *Ds =
           reinterpret_cast<const float *>(smem_gen + kOffRing + st * kStageBytes + kSDd) + col0;
       // column t is query qt*128 + col0 + t: it sees this key when it is not earlier,
-      // and exists when it is before the sequence end (the L, D of others are stale)
+      // and exists when it is before the sequence end; only the diagonal tile and a
+      // ragged last tile need the test
+      const bool masked = qt == w.kt || qt * kTile + kTile > p.T;
       const int lo = key - (qt * kTile + col0);
       const int hi = min(kTile, p.T - qt * kTile) - col0;
-#pragma unroll
-      for (int t4 = 0; t4 < 16; ++t4) {
-        const float4 L4 = *reinterpret_cast<const float4 *>(Ls + 4 * t4);
-        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 4 * t4 + e;
-          const float pr = ex2(fmaf(__uint_as_float(sr[t]), c, -Lv[e]));
-          sr[t] = __float_as_uint((t >= lo && t < hi) ? pr : 0.f);
-        }
-      }
+      if (masked)
+        key_probs<true>(sr, Ls, c, lo, hi);
+      else
+        key_probs<false>(sr, Ls, c, lo, hi);
       if (!sy.wait_warp(kBarDpFull, pos & 1, 232)) return;
       tc_fence_after();
-      uint32_t pp[32], pd[32];   // P^T and dS^T: query columns col0 + 2m, +1 in [m]
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t dr[32];
-        tmem_ld_x32(tmem + lane_base + kColDP + col0 + 32u * c2, dr);
-#pragma unroll
-        for (int t4 = 0; t4 < 8; ++t4) {
-          const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 32 * c2 + 4 * t4);
-          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-          float pv[4], dv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pv[e] = __uint_as_float(sr[32 * c2 + 4 * t4 + e]);
-            // a masked column has P = 0; its dP and D may be anything finite or not
-            dv[e] = pv[e] != 0.f ? pv[e] * (__uint_as_float(dr[4 * t4 + e]) - Dv[e]) : 0.f;
-          }
-          pp[16 * c2 + 2 * t4] = pack_half2(pv[0], pv[1]);
-          pp[16 * c2 + 2 * t4 + 1] = pack_half2(pv[2], pv[3]);
-          pd[16 * c2 + 2 * t4] = pack_half2(dv[0], dv[1]);
-          pd[16 * c2 + 2 * t4 + 1] = pack_half2(dv[2], dv[3]);
-        }
-      }
+      uint32_t pp[32], pd[32];
+      if (masked)
+        key_grads<true>(sr, Ds, tmem + lane_base + kColDP + col0, pp, pd);
+      else
+        key_grads<false>(sr, Ds, tmem + lane_base + kColDP + col0, pp, pd);
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarDpFree));
