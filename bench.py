@@ -13,6 +13,12 @@ in it.  Each launch is timed with CUDA events on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+  python bench.py --pass backward ...    # the backward pass instead (see below)
+
+The backward mode times one attn_bwd call per step (the query launch and the
+key launch) on the same workload, with O and LSE from one forward pass made
+before timing and dO from the seeded generator; it counts the five products
+of the backward, 10 * T^2 * 64 * heads / 2 FLOPs per pass.
 
 For N > 1 (torchrun), every rank runs its own independent problem of the same
 shape (weak scaling, no collective on the data path); the barrier and the
@@ -42,11 +48,14 @@ import numpy as np  # noqa: E402
 import synthetic  # noqa: E402
 
 METRIC = "causal attn fwd TFLOP/s and % of GB300 dense fp16 tensor peak, T=8192"
+METRIC_BWD = "causal attn bwd TFLOP/s (five products) and % of GB300 dense fp16 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
 KERNEL_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_fwd.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_t8192_h32_kv8.md")
+BWD_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_bwd.cu")
+BWD_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_bwd_t8192_h32_kv8.md")
 
 
 def parse_args():
@@ -58,6 +67,7 @@ def parse_args():
     ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward")
     return ap.parse_args()
 
 
@@ -197,18 +207,18 @@ def measured_peak():
         return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16; fp16 dense rate = bf16)"
 
 
-def kernel_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+def kernel_traffic(summary=TRAFFIC_SUMMARY, source=KERNEL_SOURCE, key="traffic_bytes_per_launch"):
+    """DRAM bytes per launch (or per call) from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
     try:
-        text = open(TRAFFIC_SUMMARY).read()
+        text = open(summary).read()
     except OSError:
         return None
-    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_b = re.search(key + r":\s*([0-9.eE+]+)", text)
     m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_b and m_h):
         return None
-    cur = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    cur = hashlib.sha256(open(source, "rb").read()).hexdigest()
     return float(m_b.group(1)) if cur == m_h.group(1) else None
 
 
@@ -374,9 +384,238 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- backward pass
+def bwd_flops(w):
+    """Five causal-half products of 2 * T^2/2 * 64 FLOPs per head each."""
+    return 2.5 * w.causal_flops
+
+
+def oracle_bwd_sample(w, inputs, o, lse, dO, n_rows, seed):
+    """Times the oracle on n_rows query rows (dQ) and n_rows // group key rows
+    (dK, dV); credits 384 FLOPs per causal (row, key) pair of a query row and
+    256 per (query, key) pair of a key row, the five products' split."""
+    import oracle
+    q, k, vT = inputs
+    rng = np.random.default_rng(seed)
+    qh = rng.integers(0, w.heads, n_rows)
+    qi = rng.integers(0, w.T, n_rows)
+    nk = max(1, n_rows // w.group)
+    kg = rng.integers(0, w.kv_heads, nk)
+    kj = rng.integers(0, w.T, nk)
+    t0 = time.perf_counter()
+    oracle.attn_bwd_rows(q, k, vT, o, lse, dO, w.T, w.heads, w.kv_heads, synthetic.scale_c(),
+                         0.125, qh, qi, kg, kj)
+    dt = time.perf_counter() - t0
+    fl = 384.0 * (qi + 1.0).sum() + 256.0 * w.group * (w.T - kj).astype(np.float64).sum()
+    return dt, float(fl)
+
+
+def bwd_oracle_inputs(w, inputs):
+    """The forward's O and LSE from the oracle (fp64, as the reference arm has no GPU)."""
+    import oracle
+    q, k, vT = inputs
+    return oracle.attn_fwd(q, k, vT, w.T, w.heads, w.kv_heads, synthetic.scale_c())
+
+
+def bwd_calibrate(w, inputs, o, lse, dO, target_s):
+    n = 4
+    while True:
+        dt, _ = oracle_bwd_sample(w, inputs, o, lse, dO, n, seed=1)
+        if dt > 0.5 or n >= 1 << 20:
+            break
+        n *= 4
+    return max(1, int(n * target_s / max(dt, 1e-6)))
+
+
+def run_gb300_backward(args):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        tcg_build.build()
+    if world > 1:
+        dist.barrier()
+    tcg.load_library()
+
+    base = synthetic.WORKLOADS[args.workload]
+    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    inputs = synthetic.make_inputs(w)
+    dO_np = synthetic.make_output_grad(w)
+    c, s_nat = synthetic.scale_c(), 0.125
+    T, H, G = w.T, w.heads, w.kv_heads
+    q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
+    dO = torch.from_numpy(dO_np).to(dev)
+    o = torch.empty((T, H * 64), dtype=torch.float16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    dq = torch.empty((H, T, 64), dtype=torch.float32, device=dev)
+    dk = torch.empty((G, T, 64), dtype=torch.float32, device=dev)
+    dvT = torch.empty((G, 64, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(tcg.attn_bwd_workspace_bytes(T, H, G), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    tcg.attn_fwd(q, k, vT, o, lse, T, H, G, c, stream)
+
+    def step():
+        tcg.attn_bwd(q, k, vT, o, lse, dO, dq, dk, dvT, T, H, G, c, s_nat, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    if tcg.bwd_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("backward device status after warm-up is not OK")
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid())
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if tcg.bwd_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("backward device status after the timed steps is not OK")
+    per_call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    dev_s = sum(per_call_ms) / 1e3
+
+    # end to end through the public API: pinned host inputs copied in, the call,
+    # the three gradients copied back, synchronised every step
+    host_in = [x.cpu().pin_memory() for x in (q, k, vT, o, lse, dO)]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dvT)]
+    dev_in = [torch.empty_like(x) for x in (q, k, vT, o, lse, dO)]
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        tcg.attn_bwd(*dev_in, dq, dk, dvT, T, H, G, c, s_nat, ws, stream)
+        for h, d in zip(host_out, (dq, dk, dvT)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+        stream.synchronize()
+    E = max(1, args.e2e_steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - e0
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    if rank == 0:
+        flops = bwd_flops(w)
+        avg_s = statistics.fmean(per_call_ms) / 1e3
+        achieved = flops / avg_s / 1e12
+        peak, peak_note = measured_peak()
+        line = {
+            "metric": METRIC_BWD, "value": world * K * flops / dev_s / 1e12, "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": dev_s / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": dict(workload_config(w, "flushed between timed steps (512 MiB write); "
+                                              "each call timed by CUDA events"),
+                           **{"pass": "backward"}, flops_per_step=flops,
+                           parallelism=f"independent problem per GPU x{world}"),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak,
+                         "traffic": kernel_traffic(BWD_TRAFFIC_SUMMARY, BWD_SOURCE,
+                                                   "traffic_bytes_per_call"),
+                         "peak_source": peak_note,
+                         "kernel": "attn_bwd call (query_kernel then key_kernel)",
+                         "launch_ms": {"mean": avg_s * 1e3,
+                                       "median": statistics.median(per_call_ms),
+                                       "min": min(per_call_ms)}},
+            "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "attn_bwd binding: pinned host inputs copied in, the call, "
+                            "gradients copied out, one stream, synchronised each step"},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            o_h = o.cpu().numpy()
+            l_h = lse.cpu().numpy()
+            n = bwd_calibrate(base, inputs, o_h, l_h, dO_np, 15.0)
+            dt, fl = oracle_bwd_sample(base, inputs, o_h, l_h, dO_np, n, seed=2)
+            import oracle
+            line["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+                "kind": "oracle",
+                "sample": f"{n} query rows (dQ) and {max(1, n // w.group)} key rows (dK, dV) "
+                          f"of {w.name} drawn uniformly (fp64 oracle, {dt:.1f} s); FLOPs "
+                          f"credited 384 per causal pair of a query row, 256 per pair of a "
+                          f"key row"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_backward(args):
+    import oracle
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    inputs = synthetic.make_inputs(w)
+    dO = synthetic.make_output_grad(w)
+    o, lse = bwd_oracle_inputs(w, inputs)
+    K, W = max(1, args.steps), max(3, args.warmup)
+    n = bwd_calibrate(w, inputs, o, lse, dO, 120.0 / (K + W))
+    for i in range(W):
+        oracle_bwd_sample(w, inputs, o, lse, dO, n, seed=100 + i)
+    tot_s = tot_fl = 0.0
+    for i in range(K):
+        dt, fl = oracle_bwd_sample(w, inputs, o, lse, dO, n, seed=1000 + i)
+        tot_s += dt
+        tot_fl += fl
+    value = tot_fl / tot_s / 1e12
+    sample = (f"each step: {n} query rows (dQ) and {max(1, n // w.group)} key rows (dK, dV) of "
+              f"{w.name}; FLOPs credited 384 per causal pair of a query row, 256 per pair of a "
+              f"key row")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": tot_s / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": dict(workload_config(w, "not applicable (host CPU)"), **{"pass": "backward"},
+                       parallelism="host cores of rank 0"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.which == "backward":
+        (run_reference_backward if args.impl == "reference" else run_gb300_backward)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gb300(args)

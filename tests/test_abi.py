@@ -103,3 +103,58 @@ def test_binding_checks_tensors(lib):
     q = torch.zeros(4, 128, 64, dtype=torch.float32)
     with pytest.raises(TypeError):
         tcg.attn_fwd(q, q, q, q, q, 128, 4, 2, 0.18)
+
+
+# ---------------------------------------------------------------------------- backward entry
+def bwd_call(lib, T=128, H=4, G=2, c=0.18, s=0.125, ws_bytes=None, **ptr):
+    """attn_bwd with fake, well-separated device addresses (no launch happens on a
+    rejected call).  Sizes at T=128, H=4, G=2: q/o/dO 64 KiB, k/vT 32 KiB, lse 2 KiB,
+    dq 128 KiB, dk/dvT 64 KiB, workspace 2 KiB."""
+    base = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, l=0x500000, g=0x600000,
+                dq=0x700000, dk=0x800000, dv=0x900000, ws=0xA00000)
+    base.update(ptr)
+    vp = ctypes.c_void_p
+    if ws_bytes is None:
+        ws_bytes = tcg.attn_bwd_workspace_bytes(T, H, G) if T > 0 and T % 64 == 0 else 1 << 20
+    return lib.attn_bwd(vp(base["q"]), vp(base["k"]), vp(base["v"]), vp(base["o"]),
+                        vp(base["l"]), vp(base["g"]), vp(base["dq"]), vp(base["dk"]),
+                        vp(base["dv"]), T, H, G, c, s, vp(base["ws"]), ws_bytes, None)
+
+
+@pytest.mark.parametrize("T,H,G,c,s", [
+    (0, 4, 2, 0.18, 0.125), (100, 4, 2, 0.18, 0.125), (128, 4, 3, 0.18, 0.125),
+    (128, 65536, 1, 0.18, 0.125), (2 ** 24, 1, 1, 0.18, 0.125),
+    (128, 4, 2, 0.0, 0.125), (128, 4, 2, 0.18, 0.0), (128, 4, 2, 0.18, float("nan")),
+    (128, 4, 2, float("inf"), 0.125), (128, 4, 2, 0.18, -1.0),
+])
+def test_bwd_rejects_inadmissible_shapes(lib, T, H, G, c, s):
+    assert bwd_call(lib, T=T, H=H, G=G, c=c, s=s) == tcg.ATTN_EINVAL
+
+
+def test_bwd_rejects_null_misaligned_short_workspace(lib):
+    assert bwd_call(lib, g=0) == tcg.ATTN_EINVAL
+    assert bwd_call(lib, ws=0) == tcg.ATTN_EINVAL
+    assert bwd_call(lib, dq=0x700008) == tcg.ATTN_EALIGN
+    assert bwd_call(lib, l=0x500004) == tcg.ATTN_EALIGN
+    assert bwd_call(lib, ws=0xA00010) == tcg.ATTN_EALIGN          # workspace wants 256 bytes
+    assert bwd_call(lib, ws_bytes=tcg.attn_bwd_workspace_bytes(128, 4, 2) - 1) == tcg.ATTN_EINVAL
+
+
+def test_bwd_rejects_overlaps(lib):
+    assert bwd_call(lib, dq=0x100000 + 65536 - 16) == tcg.ATTN_EOVERLAP      # dq over q
+    assert bwd_call(lib, dk=0x700000 + 131072 - 16) == tcg.ATTN_EOVERLAP     # dk over dq
+    assert bwd_call(lib, ws=0x900000) == tcg.ATTN_EOVERLAP                   # workspace over dvT
+    assert bwd_call(lib, dv=0x600000 + 65536) != tcg.ATTN_EOVERLAP           # adjacent is fine
+
+
+def test_bwd_workspace_bytes(lib):
+    assert tcg.attn_bwd_workspace_bytes(8192, 32, 8) == 32 * 8192 * 4
+    assert tcg.attn_bwd_workspace_bytes(64, 3, 1) == 768        # T % 64 == 0: already 256-aligned
+    assert tcg.attn_bwd_workspace_bytes(100, 4, 2) == 0
+
+
+def test_bwd_binding_checks_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 128, 64, dtype=torch.float16)
+    with pytest.raises((TypeError, ValueError)):
+        tcg.attn_bwd(x, x, x, x, x, x, x, x, x, 128, 4, 2, 0.18, 0.125, x)
