@@ -158,3 +158,39 @@ def test_bwd_binding_checks_tensors(lib):
     x = torch.zeros(4, 128, 64, dtype=torch.float16)
     with pytest.raises((TypeError, ValueError)):
         tcg.attn_bwd(x, x, x, x, x, x, x, x, x, 128, 4, 2, 0.18, 0.125, x)
+
+
+# ---------------------------------------------------------------------------- materialised entry
+def mat_call(lib, T=128, H=4, G=2, c=0.18, ws_bytes=None, **ptr):
+    """attn_fwd_materialised with fake, well-separated device addresses (no launch
+    happens on a rejected call).  At T=128, H=4, G=2: q/o 64 KiB, k/vT 32 KiB, lse 2 KiB,
+    workspace 384 KiB."""
+    base = dict(q=0x100000, k=0x200000, v=0x300000, o=0x400000, l=0x500000, ws=0x600000)
+    base.update(ptr)
+    vp = ctypes.c_void_p
+    if ws_bytes is None:
+        ws_bytes = tcg.attn_materialised_workspace_bytes(T, H, G) or (1 << 20)
+    return lib.attn_fwd_materialised(vp(base["q"]), vp(base["k"]), vp(base["v"]), vp(base["o"]),
+                                     vp(base["l"]), T, H, G, c, vp(base["ws"]), ws_bytes, None)
+
+
+@pytest.mark.parametrize("T,H,G,c", [
+    (0, 4, 2, 0.18), (100, 4, 2, 0.18), (128, 4, 3, 0.18), (16384 + 64, 1, 1, 0.18),
+    (128, 4, 2, 0.0), (128, 4, 2, float("nan")),
+])
+def test_mat_rejects_inadmissible_shapes(lib, T, H, G, c):
+    assert mat_call(lib, T=T, H=H, G=G, c=c) == tcg.ATTN_EINVAL
+
+
+def test_mat_rejects_bad_pointers_and_workspace(lib):
+    assert mat_call(lib, q=0) == tcg.ATTN_EINVAL
+    assert mat_call(lib, ws=0x600010) == tcg.ATTN_EALIGN
+    assert mat_call(lib, ws_bytes=tcg.attn_materialised_workspace_bytes(128, 4, 2) - 1) == tcg.ATTN_EINVAL
+    assert mat_call(lib, o=0x100000 + 65536 - 16) == tcg.ATTN_EOVERLAP      # o over q
+    assert mat_call(lib, ws=0x400000) == tcg.ATTN_EOVERLAP                  # workspace over o
+
+
+def test_mat_workspace_bytes(lib):
+    assert tcg.attn_materialised_workspace_bytes(1024, 12, 12) == 12 * 1024 * 1024 * 6
+    assert tcg.attn_materialised_workspace_bytes(16384, 1, 1) == 16384 * 16384 * 6
+    assert tcg.attn_materialised_workspace_bytes(16384 + 64, 1, 1) == 0

@@ -2,7 +2,7 @@
 streaming normalised sum, and its backward pass.
 
 A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h`` and
-``include/attn_bwd.h`` (``libattn_gb300.so``): it checks tensor dtypes,
+``include/attn_bwd.h`` and ``include/attn_materialised.h`` (``libattn_gb300.so``): it checks tensor dtypes,
 devices and contiguity, and passes raw pointers, sizes and the stream handle.
 Every step of both passes runs in the library's CUDA kernels; there is no CPU
 path.  If the library has not been built, every entry point raises
@@ -32,11 +32,12 @@ ATTN_ELAUNCH = -4
 ATTN_EDEVICE = -5
 ATTN_ETIMEOUT = -6
 
-# every symbol include/attn_fwd.h and include/attn_bwd.h declare
+# every symbol the headers under include/ declare
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
             "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_bwd_last_device_status")
+            "attn_bwd_last_device_status", "attn_fwd_materialised",
+            "attn_materialised_workspace_bytes", "attn_materialised_last_device_status")
 
 _lib = None
 
@@ -82,6 +83,12 @@ def load_library():
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd_last_device_status.argtypes = [vp]
     lib.attn_bwd_last_device_status.restype = i
+    lib.attn_fwd_materialised.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp, sz, vp]
+    lib.attn_fwd_materialised.restype = i
+    lib.attn_materialised_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_materialised_workspace_bytes.restype = sz
+    lib.attn_materialised_last_device_status.argtypes = [vp]
+    lib.attn_materialised_last_device_status.restype = i
     _lib = lib
     return lib
 
@@ -240,3 +247,34 @@ def attention_backward(q, k, vT, o, lse, dO, c: float, s: float, stream=None):
                      device=q.device)
     attn_bwd(q, k, vT, o, lse, dO, dq, dk, dvT, T, heads, kv_heads, c, s, ws, stream)
     return dq, dk, dvT
+
+
+def attn_materialised_workspace_bytes(T: int, heads: int, kv_heads: int) -> int:
+    return int(load_library().attn_materialised_workspace_bytes(int(T), int(heads), int(kv_heads)))
+
+
+def attn_fwd_materialised(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
+                          workspace, stream=None) -> None:
+    """The forward through materialised scores and probability planes (the design the
+    streaming kernel replaces), on CUDA tensors; ``workspace`` is a CUDA uint8 tensor of
+    at least attn_materialised_workspace_bytes bytes."""
+    import torch
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T))
+    _check_tensor("o", o, torch.float16, (T, heads * HEAD_DIM))
+    _check_tensor("lse", lse, torch.float32, (heads, T))
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace: must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().attn_fwd_materialised(q.data_ptr(), k.data_ptr(), vT.data_ptr(),
+                                              o.data_ptr(), lse.data_ptr(), int(T), int(heads),
+                                              int(kv_heads), float(c), workspace.data_ptr(),
+                                              nbytes, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_materialised")
+
+
+def materialised_last_device_status(stream=None) -> int:
+    """Synchronises ``stream``; ATTN_OK, or ATTN_ETIMEOUT if a materialised-path wait gave up."""
+    return int(load_library().attn_materialised_last_device_status(_stream_handle(stream)))
