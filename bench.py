@@ -15,6 +15,11 @@ in it.  Each launch is timed with CUDA events on the launching stream.
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
   python bench.py --pass backward ...    # the backward pass instead (see below)
 
+The materialised mode (--pass materialised) times one attn_fwd_materialised
+call per step: the same forward through a binary32 scores plane and a
+binary16 probability plane (three launches), reported in the same causal
+TFLOP/s and against the HBM roofline, since it moves the planes through memory.
+
 The backward mode times one attn_bwd call per step (the query launch and the
 key launch) on the same workload, with O and LSE from one forward pass made
 before timing and dO from the seeded generator; it counts the five products
@@ -49,6 +54,7 @@ import synthetic  # noqa: E402
 
 METRIC = "causal attn fwd TFLOP/s and % of GB300 dense fp16 tensor peak, T=8192"
 METRIC_BWD = "causal attn bwd TFLOP/s (five products) and % of GB300 dense fp16 tensor peak"
+METRIC_MAT = "materialised causal attn fwd TFLOP/s (scores + probability planes), HBM roofline"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
@@ -67,7 +73,8 @@ def parse_args():
     ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="which", choices=["forward", "backward"], default="forward")
+    ap.add_argument("--pass", dest="which", choices=["forward", "backward", "materialised"],
+                    default="forward")
     return ap.parse_args()
 
 
@@ -351,7 +358,7 @@ def run_gb300(args):
 
 
 # ----------------------------------------------------------------------------- reference arm
-def run_reference(args):
+def run_reference(args, metric=METRIC):
     import oracle
     rank, _, world = dist_env()
     if rank != 0:
@@ -372,7 +379,7 @@ def run_reference(args):
     sample = (f"each step: {rows} query rows of {w.name} drawn uniformly over heads and rows; "
               f"FLOPs credited 256 per causal (row, key) pair as in the metric")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": tot_s / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(workload_config(w, "not applicable (host CPU)"),
@@ -611,9 +618,171 @@ def run_reference_backward(args):
     }), flush=True)
 
 
+# ----------------------------------------------------------------------------- materialised path
+def measured_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def materialised_bytes(w):
+    """Algorithmic DRAM bytes of one attn_fwd_materialised call: the scores plane's
+    causal tiles written once and their causal elements read once, the probability
+    plane written up to each row's diagonal-tile end and its causal tiles read once,
+    plus Q, K, V^T read and O, LSE written once."""
+    T, H, G = w.T, w.heads, w.kv_heads
+    nt = (T + 127) // 128
+    tile_elems = 0
+    for qt in range(nt):
+        rows = min(128, T - 128 * qt)
+        for kt in range(qt + 1):
+            tile_elems += rows * min(128, T - 128 * kt)
+    causal = T * (T + 1) // 2
+    p_written = sum(min(T, (i // 128 + 1) * 128) for i in range(T))
+    io = 2 * H * T * 64 + 2 * 2 * G * T * 64 + 2 * T * H * 64 + 4 * H * T
+    return H * (4 * tile_elems + 4 * causal + 2 * p_written + 2 * tile_elems) + io
+
+
+def run_gb300_materialised(args):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        tcg_build.build()
+    if world > 1:
+        dist.barrier()
+    tcg.load_library()
+    base = synthetic.WORKLOADS[args.workload]
+    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    inputs = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    T, H, G = w.T, w.heads, w.kv_heads
+    q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
+    o = torch.empty((T, H * 64), dtype=torch.float16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    ws = torch.empty(tcg.attn_materialised_workspace_bytes(T, H, G), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tcg.attn_fwd_materialised(q, k, vT, o, lse, T, H, G, c, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    if tcg.materialised_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("materialised device status after warm-up is not OK")
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid())
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if tcg.materialised_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("materialised device status after the timed steps is not OK")
+    per_call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    dev_s = sum(per_call_ms) / 1e3
+
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in inputs)
+    oh = torch.empty((T, H * 64), dtype=torch.float16).pin_memory()
+    lh = torch.empty((H, T), dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(vT)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        tcg.attn_fwd_materialised(qd, kd, vd, o, lse, T, H, G, c, ws, stream)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+        stream.synchronize()
+    E = max(1, args.e2e_steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - e0
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    if rank == 0:
+        flops = w.causal_flops
+        avg_s = statistics.fmean(per_call_ms) / 1e3
+        nbytes = materialised_bytes(w)
+        peak, peak_note = measured_hbm()
+        achieved = nbytes / avg_s / 1e9
+        line = {
+            "metric": METRIC_MAT, "value": world * K * flops / dev_s / 1e12, "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": dev_s / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": dict(workload_config(w, "flushed between timed steps (512 MiB write); "
+                                              "each call timed by CUDA events"),
+                           **{"pass": "materialised"}, algorithmic_bytes_per_step=nbytes,
+                           workspace_bytes=ws.numel(),
+                           parallelism=f"independent problem per GPU x{world}"),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_note,
+                         "kernel": "attn_fwd_materialised call (scores, softmax, pv kernels)",
+                         "launch_ms": {"mean": avg_s * 1e3,
+                                       "median": statistics.median(per_call_ms),
+                                       "min": min(per_call_ms)}},
+            "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "attn_fwd_materialised binding: pinned host inputs copied in, the "
+                            "call, O and LSE copied out, synchronised each step"},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(base, inputs)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
-    if args.which == "backward":
+    if args.which == "materialised":
+        if args.impl == "reference":
+            run_reference(args, metric=METRIC_MAT)
+        else:
+            run_gb300_materialised(args)
+    elif args.which == "backward":
         (run_reference_backward if args.impl == "reference" else run_gb300_backward)(args)
     elif args.impl == "reference":
         run_reference(args)
