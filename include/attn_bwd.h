@@ -93,6 +93,19 @@ int attn_bwd(const void *q, const void *k, const void *vT, const void *o,
  */
 int attn_bwd_last_device_status(cudaStream_t stream);
 
+/*
+ * attn_bwd_test_inject_stall -- test hook for the backward's failure detection.
+ *
+ * The source pages have no counterpart of this entry point.  It makes the
+ * next attn_bwd call's query launch skip the first K/V copy of its first CTA.
+ * The wait on that copy runs out after 1 s: the CTA records a timeout, drains
+ * what it issued, frees its tensor memory and exits; the key launch runs as
+ * usual (on that CTA's missing row terms, so the call's outputs are not
+ * valid); attn_bwd_last_device_status then returns ATTN_ETIMEOUT, and later
+ * calls run normally.  Always returns ATTN_OK.
+ */
+int attn_bwd_test_inject_stall(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -129,7 +129,7 @@ def sampled_rows(T, n, rng):
     return np.concatenate([np.array(fixed), extra]).astype(np.int64)
 
 
-@pytest.mark.parametrize("name", [synthetic.HEADLINE])
+@pytest.mark.parametrize("name", [synthetic.HEADLINE, "t16384_h64_kv8_outliers"])
 def test_full_size_sampled_rows(name):
     w = synthetic.WORKLOADS[name]
     q, k, vT = synthetic.make_inputs(w)

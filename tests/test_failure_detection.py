@@ -42,3 +42,33 @@ def test_wait_runs_out_then_recovers():
     o_ref, lse_ref = oracle.attn_fwd(q, k, vT, w.T, w.heads, w.kv_heads, c)
     assert float(np.abs(o.cpu().numpy().astype(np.float64) - o_ref).max()) <= 4e-3
     assert float(np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max()) <= 1e-3
+
+
+def test_backward_wait_runs_out_then_recovers():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tcg_build.build()
+    lib = tcg.load_library()
+    w = synthetic.custom(512, 8, 2, seed=32)
+    q, k, vT = synthetic.make_inputs(w)
+    dO = synthetic.make_output_grad(w)
+    c = synthetic.scale_c()
+    dev = torch.device("cuda:0")
+    qd, kd, vd, gd = (torch.from_numpy(x).to(dev) for x in (q, k, vT, dO))
+    o, lse = tcg.attention(qd, kd, vd, c)
+    assert tcg.last_device_status() == tcg.ATTN_OK
+    good = [x.cpu() for x in tcg.attention_backward(qd, kd, vd, o, lse, gd, c, 0.125)]
+    assert tcg.bwd_last_device_status() == tcg.ATTN_OK
+
+    assert lib.attn_bwd_test_inject_stall() == tcg.ATTN_OK
+    t0 = time.monotonic()
+    tcg.attention_backward(qd, kd, vd, o, lse, gd, c, 0.125)
+    assert tcg.bwd_last_device_status() == tcg.ATTN_ETIMEOUT
+    assert time.monotonic() - t0 < 10.0
+    assert tcg.bwd_last_device_status() == tcg.ATTN_OK    # reading it cleared it
+
+    # the context is usable and the next call reproduces the good result bit for bit
+    again = [x.cpu() for x in tcg.attention_backward(qd, kd, vd, o, lse, gd, c, 0.125)]
+    assert tcg.bwd_last_device_status() == tcg.ATTN_OK
+    for a, b in zip(good, again):
+        assert torch.equal(a, b)

@@ -36,7 +36,7 @@ ATTN_ETIMEOUT = -6
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
             "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_bwd_last_device_status", "attn_fwd_materialised",
+            "attn_bwd_last_device_status", "attn_bwd_test_inject_stall", "attn_fwd_materialised",
             "attn_materialised_workspace_bytes", "attn_materialised_last_device_status")
 
 _lib = None
@@ -83,6 +83,8 @@ def load_library():
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd_last_device_status.argtypes = [vp]
     lib.attn_bwd_last_device_status.restype = i
+    lib.attn_bwd_test_inject_stall.argtypes = []
+    lib.attn_bwd_test_inject_stall.restype = i
     lib.attn_fwd_materialised.argtypes = [vp, vp, vp, vp, vp, i, i, i, f, vp, sz, vp]
     lib.attn_fwd_materialised.restype = i
     lib.attn_materialised_workspace_bytes.argtypes = [i, i, i]

@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -109,6 +110,7 @@ struct BwdParams {
   float *dk;          // [G][T][64]
   float *dvT;         // [G][64][T]
   int *status;
+  int stall;          // test hook: CTA 0 of the query launch never loads its first K/V stage
 };
 
 // k-th unit of this CTA (static, serpentine over the grid; units are numbered
@@ -181,6 +183,7 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const
       const uint32_t full = sy.bar(kBarKvFull + st);
       mbar_arrive_expect_tx(full, kStageBytes);
       pos_issued = pos + 1;
+      if (p.stall && blockIdx.x == 0 && pos == 0) continue;   // this stage never lands
       tma_load_3d(dst, tmK, full, 0, j * kTile, w.g);
       tma_load_3d(dst + kTileBytes, tmVT, full, j * kTile, 0, w.g);
       tma_load_3d(dst + kTileBytes + kHalfTileBytes, tmVT, full, j * kTile + kTile / 2, 0, w.g);
@@ -791,6 +794,7 @@ struct BwdState {
 };
 std::mutex g_bwd_mutex;
 BwdState g_bwd[64];
+std::atomic<int> g_bwd_stall{0};   // test hook: the next attn_bwd call stalls one CTA
 PFN_cuTensorMapEncodeTiled_v12000 g_bwd_encode = nullptr;
 
 int bwd_state(BwdState **out) {
@@ -924,6 +928,7 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   p.dk = dk;
   p.dvT = dvT;
   p.status = st->status;
+  p.stall = g_bwd_stall.exchange(0);
   const int qunits = heads * p.q_tiles, kunits = kv_heads * p.q_tiles;
   qlaunch::query_kernel<<<qunits < st->sms ? qunits : st->sms, qlaunch::kThreads,
                           qlaunch::kSmemBytes, stream>>>(tmQ, tmDO, tmK, tmVT, p);
@@ -943,4 +948,9 @@ extern "C" int attn_bwd_last_device_status(cudaStream_t stream) {
     return ATTN_ELAUNCH;
   if (word != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
   return word ? ATTN_ETIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_bwd_test_inject_stall(void) {
+  g_bwd_stall.store(1);
+  return ATTN_OK;
 }
