@@ -33,6 +33,8 @@
 #include "attn_bwd.h"
 #include "sm103_ptx.cuh"
 
+
+
 namespace {
 
 using namespace sm103;
@@ -126,9 +128,11 @@ __device__ __forceinline__ int unit_of(int k, int units) {
 // Unit = (query head h, 128-row query tile qt), latest (heaviest) tiles first;
 // key tiles 0 .. qt.  Eight compute warps: warp w serves tensor-memory lanes
 // 32 (w % 4) .. +31 (one query row per thread) and key columns 64 (w / 4) ..
-// +63 of each tile.  Tensor memory: S in two buffers at 0 and 128 (so S of
-// the next tile is formed while this one is processed), dP at 256 (fp32),
-// dS at 384 (binary16 pairs, 64 columns), dQ at 448 (fp32, 64 columns).
+// +63 of each tile.  A step loads its S and dP rows with one wait, releases
+// both at once (so the next pair is formed while this one is processed), and
+// forms P and dS in one pass.  Tensor memory: S at 0, dP at 128 (fp32), dS in
+// two buffers at 256 and 320 (binary16 pairs, so a step need not wait for the
+// previous dQ product), dQ at 384 (fp32, 64 columns).
 namespace qlaunch {
 constexpr int kStages = 4;                       // ring of {K tile, V^T tile}
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
@@ -137,15 +141,14 @@ constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarQFull = 0, kBarQEmpty = 1;
 constexpr int kBarKvFull = 2, kBarKvEmpty = 2 + kStages;
-constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 2;   // two each
-constexpr int kBarDpFull = kBarSFree + 2, kBarDpFree = kBarDpFull + 1;
-constexpr int kBarDsFull = kBarDpFree + 1, kBarDqDone = kBarDsFull + 1;
-constexpr int kBarDrain = kBarDqDone + 1;        // + issuer warp (0, 1)
+constexpr int kBarSdFull = 2 + 2 * kStages, kBarSdFree = kBarSdFull + 1;
+constexpr int kBarDsFull = kBarSdFree + 1, kBarDqDone = kBarDsFull + 2;   // two each
+constexpr int kBarDrain = kBarDqDone + 2;        // + issuer warp (0, 1)
 constexpr int kNumBars = kBarDrain + 2;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
-constexpr uint32_t kColS = 0, kColDP = 256, kColDS = 384, kColDQ = 448;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;
 constexpr int kComputeWarps = 8;
 constexpr int kWarpSdp = 8, kWarpDq = 9, kWarpLoad = 10;
 constexpr int kThreads = 32 * 11;
@@ -162,7 +165,6 @@ __device__ __forceinline__ Unit decode(int u, const BwdParams &p) {
   w.nk = w.qt + 1;
   return w;
 }
-
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const CUtensorMap *tmK,
                           const CUtensorMap *tmVT, const BwdParams &p, const Sync &sy,
                           uint32_t smem) {
@@ -198,8 +200,8 @@ drain:
   if (q_issued > 0) sy.drain_wait(kBarQFull, (q_issued - 1) & 1);
 }
 
-// S = Q K^T (both K-major) into the S buffer of the tile's parity, then
-// dP = dO V^T (B read MN-major from the V^T tile: 64-key halves 8 KiB apart).
+// S = Q K^T and dP = dO V^T for one key tile, once the compute warps have
+// pulled the previous pair into registers; one commit for both.
 __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kTile, kTile);
   constexpr uint32_t idDP = idesc_f16_f32_mn(kTile, kTile, false, true);
@@ -211,23 +213,20 @@ __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint
     if (!sy.wait_warp(kBarQFull, k & 1, 111)) goto drain;
     tc_fence_after();
     for (int j = 0; j < w.nk; ++j, ++pos) {
-      const uint32_t st = pos % kStages, b = pos & 1;
+      const uint32_t st = pos % kStages;
       if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 112)) goto drain;
-      if (!sy.wait_warp(kBarSFree + b, ((pos >> 1) & 1) ^ 1, 113)) goto drain;
+      if (!sy.wait_warp(kBarSdFree, (pos & 1) ^ 1, 113)) goto drain;
       tc_fence_after();
       const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
-        mma_ss(tmem + kColS + 128u * b, sw128_desc(smem + kOffQ + e * 32), sw128_desc(kb + e * 32),
-               idS, e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarSFull + b));
-      if (!sy.wait_warp(kBarDpFree, (pos & 1) ^ 1, 114)) goto drain;
-      tc_fence_after();
+        mma_ss(tmem + kColS, sw128_desc(smem + kOffQ + e * 32), sw128_desc(kb + e * 32), idS,
+               e > 0 ? 1u : 0u);
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
         mma_ss(tmem + kColDP, sw128_desc(smem + kOffQ + kTileBytes + e * 32),
                sw128_mn_desc(kb + kTileBytes + e * 2048, kHalfTileBytes), idDP, e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarDpFull));
+      mma_commit(sy.bar(kBarSdFull));
       mma_commit(sy.bar(kBarKvEmpty + st));
     }
     mma_commit(sy.bar(kBarQEmpty));
@@ -238,7 +237,7 @@ drain:
   sy.drain_wait(kBarDrain + 0, 0);
 }
 
-// dQ += dS K (A = dS from tensor memory; B read MN-major from the K tile).
+// dQ += dS K (A = dS from one of two tensor-memory buffers; B MN-major from the K tile).
 __device__ void dq_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t id = idesc_f16_f32_mn(kTile, kD, false, true);
   const int units = p.heads * p.q_tiles;
@@ -247,16 +246,16 @@ __device__ void dq_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint3
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
     for (int j = 0; j < w.nk; ++j, ++pos) {
-      const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarDsFull, pos & 1, 121)) goto drain;
+      const uint32_t st = pos % kStages, b = pos & 1;
+      if (!sy.wait_warp(kBarDsFull + b, (pos >> 1) & 1, 121)) goto drain;
       if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 122)) goto drain;
       tc_fence_after();
       const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
       for (int e = 0; e < kTile / 16; ++e)
-        mma_ts(tmem + kColDQ, tmem + kColDS + 8u * e, sw128_mn_desc(kb + e * 2048, kHalfTileBytes),
-               id, (j > 0 || e > 0) ? 1u : 0u);
-      mma_commit(sy.bar(kBarDqDone));
+        mma_ts(tmem + kColDQ, tmem + kColDS + 64u * b + 8u * e,
+               sw128_mn_desc(kb + e * 2048, kHalfTileBytes), id, (j > 0 || e > 0) ? 1u : 0u);
+      mma_commit(sy.bar(kBarDqDone + b));
       mma_commit(sy.bar(kBarKvEmpty + st));
     }
   }
@@ -307,54 +306,46 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
     const float negL = -L;
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t b = pos & 1;
-      if (!sy.wait_warp(kBarSFull + b, (pos >> 1) & 1, 131)) return;
+      if (!sy.wait_warp(kBarSdFull, pos & 1, 131)) return;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld_x64(tmem + lane_base + kColS + 128u * b + col0, sr);
+      uint32_t sr[64], dr[64];
+      tmem_ld_2x64(tmem + lane_base + kColS + col0, tmem + lane_base + kColDP + col0, sr, dr);
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarSFree + b));
-      // P = 2^(S c - L); on the diagonal tile keys after the row get P = 0
+      if (leader) mbar_arrive(sy.bar(kBarSdFree));
+      // P = 2^(S c - L) and dS = P (dP - D) in one pass, packed to binary16 pairs
+      // (key columns col0 + 2m, +1 in pk[m]); on the diagonal tile keys after the
+      // row get P = 0
+      uint32_t pk[32];
       if (j == w.qt) {
         const int lim = r - col0;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float pr = ex2(fmaf(__uint_as_float(sr[i]), c, negL));
-          sr[i] = __float_as_uint(i <= lim ? pr : 0.f);
+        for (int i = 0; i < 32; ++i) {
+          float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, negL));
+          float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, negL));
+          if (2 * i > lim) p0 = 0.f;
+          if (2 * i + 1 > lim) p1 = 0.f;
+          pk[i] = pack_half2(p0 * (__uint_as_float(dr[2 * i]) - D), p1 * (__uint_as_float(dr[2 * i + 1]) - D));
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sr[i] = __float_as_uint(ex2(fmaf(__uint_as_float(sr[i]), c, negL)));
-      }
-      if (!sy.wait_warp(kBarDpFull, pos & 1, 132)) return;
-      tc_fence_after();
-      uint32_t pk[32];   // dS: key columns col0 + 2m, +1 in pk[m]
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t dr[32];
-        tmem_ld_x32(tmem + lane_base + kColDP + col0 + 32u * c2, dr);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float ds0 = __uint_as_float(sr[32 * c2 + 2 * i]) * (__uint_as_float(dr[2 * i]) - D);
-          const float ds1 =
-              __uint_as_float(sr[32 * c2 + 2 * i + 1]) * (__uint_as_float(dr[2 * i + 1]) - D);
-          pk[16 * c2 + i] = pack_half2(ds0, ds1);
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, negL));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, negL));
+          pk[i] = pack_half2(p0 * (__uint_as_float(dr[2 * i]) - D), p1 * (__uint_as_float(dr[2 * i + 1]) - D));
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarDpFree));
-      if (j > 0) {   // dS(j-1) K must be complete before dS is overwritten
-        if (!sy.wait_warp(kBarDqDone, (pos - 1) & 1, 133)) return;
+      if (pos >= 2) {   // the product that read this dS buffer two steps ago must be complete
+        if (!sy.wait_warp(kBarDqDone + b, ((pos >> 1) & 1) ^ 1, 133)) return;
         tc_fence_after();
       }
-      tmem_st_x32(tmem + lane_base + kColDS + 32u * half, pk);
+      tmem_st_x32(tmem + lane_base + kColDS + 64u * b + 32u * half, pk);
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarDsFull));
+      if (leader) mbar_arrive(sy.bar(kBarDsFull + b));
     }
     // epilogue: dQ = s (sum) once the last product is done; each half writes 32 columns
-    if (!sy.wait_warp(kBarDqDone, (pos - 1) & 1, 134)) return;
+    if (!sy.wait_warp(kBarDqDone + ((pos - 1) & 1), ((pos - 1) >> 1) & 1, 134)) return;
     tc_fence_after();
     uint32_t qr[32];
     tmem_ld_x32(tmem + lane_base + kColDQ + 32u * half, qr);
@@ -389,14 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sy.bar(kBarKvFull + i), 1);
       mbar_init(sy.bar(kBarKvEmpty + i), 2);   // S/dP issuer and dQ issuer
     }
+    mbar_init(sy.bar(kBarSdFull), 1);
+    mbar_init(sy.bar(kBarSdFree), kComputeWarps);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(sy.bar(kBarSFull + i), 1);
-      mbar_init(sy.bar(kBarSFree + i), kComputeWarps);
+      mbar_init(sy.bar(kBarDsFull + i), kComputeWarps);
+      mbar_init(sy.bar(kBarDqDone + i), 1);
     }
-    mbar_init(sy.bar(kBarDpFull), 1);
-    mbar_init(sy.bar(kBarDpFree), kComputeWarps);
-    mbar_init(sy.bar(kBarDsFull), kComputeWarps);
-    mbar_init(sy.bar(kBarDqDone), 1);
     mbar_init(sy.bar(kBarDrain + 0), 1);
     mbar_init(sy.bar(kBarDrain + 1), 1);
     *sy.abort_flag = 0;
@@ -434,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // unit steps through every query head z of the group and, for each, the
 // query tiles kt .. q_tiles-1, accumulating dK and dV over all of them.
 // Eight compute warps: warp w serves lanes 32 (w % 4) .. +31 (one key per
-// thread) and query columns 64 (w / 4) .. +63.  Tensor memory: S^T at 0,
+// thread) and query columns 64 (w / 4) .. +63; as in the query launch, S^T
+// and dP^T arrive and are released together.  Tensor memory: S^T at 0,
 // dP^T at 128 (fp32), P^T at 256, dS^T at 320 (binary16 pairs), dV at 384,
 // dK at 448 (fp32).
 namespace klaunch {
@@ -445,9 +435,8 @@ constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarKvFull = 0, kBarKvEmpty = 1;
 constexpr int kBarQFull = 2, kBarQEmpty = 2 + kStages;
-constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 1;
-constexpr int kBarDpFull = kBarSFree + 1, kBarDpFree = kBarDpFull + 1;
-constexpr int kBarPFull = kBarDpFree + 1, kBarDvDone = kBarPFull + 1, kBarDkDone = kBarDvDone + 1;
+constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 1;   // S^T and dP^T together
+constexpr int kBarPFull = kBarSFree + 1, kBarDvDone = kBarPFull + 1, kBarDkDone = kBarDvDone + 1;
 constexpr int kBarDrain = kBarDkDone + 1;        // + issuer warp (0..2)
 constexpr int kNumBars = kBarDrain + 3;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
@@ -540,14 +529,11 @@ __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint
       for (int e = 0; e < kD / 16; ++e)
         mma_ss(tmem + kColS, sw128_desc(smem + kOffK + e * 32), sw128_desc(sb + kSQ + e * 32), idS,
                e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarSFull));
-      if (!sy.wait_warp(kBarDpFree, (pos & 1) ^ 1, 214)) goto drain;
-      tc_fence_after();
 #pragma unroll
       for (int e = 0; e < kD / 16; ++e)
         mma_ss(tmem + kColDP, sw128_mn_desc(smem + kOffK + kTileBytes + e * 2048, kHalfTileBytes),
                sw128_desc(sb + kSDO + e * 32), idDP, e > 0 ? 1u : 0u);
-      mma_commit(sy.bar(kBarDpFull));
+      mma_commit(sy.bar(kBarSFull));
       mma_commit(sy.bar(kBarQEmpty + st));
     }
     mma_commit(sy.bar(kBarKvEmpty));
@@ -592,52 +578,32 @@ drain:
   sy.drain_wait(kBarDrain + 1 + which, 0);
 }
 
-// P^T = 2^(S^T c - L) over the thread's 64 query columns (in place).  With
-// kMasked, column t is kept only when lo <= t < hi: the query is not earlier
-// than the key and exists (columns past the sequence end carry stale L, D).
+// One key row's step over the thread's 64 query columns: P^T = 2^(S^T c - L)
+// and dS^T = P^T (dP^T - D), packed to binary16 pairs (query columns 2m,
+// 2m+1 in [m]).  With kMasked, column t is kept only when lo <= t < hi.
 template <bool kMasked>
-__device__ __forceinline__ void key_probs(uint32_t (&sr)[64], const float *Ls, float c, int lo,
-                                          int hi) {
+__device__ __forceinline__ void key_step(const uint32_t (&sr)[64], const uint32_t (&dr)[64],
+                                         const float *Ls, const float *Ds, float c, int lo, int hi,
+                                         uint32_t (&pp)[32], uint32_t (&pd)[32]) {
 #pragma unroll
   for (int t4 = 0; t4 < 16; ++t4) {
     const float4 L4 = *reinterpret_cast<const float4 *>(Ls + 4 * t4);
-    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+    const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 4 * t4);
+    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+    float pv[4], dv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int t = 4 * t4 + e;
       const float pr = ex2(fmaf(__uint_as_float(sr[t]), c, -Lv[e]));
-      sr[t] = __float_as_uint(!kMasked || (t >= lo && t < hi) ? pr : 0.f);
+      const float g = pr * (__uint_as_float(dr[t]) - Dv[e]);
+      const bool live = !kMasked || (t >= lo && t < hi);
+      pv[e] = live ? pr : 0.f;
+      dv[e] = live ? g : 0.f;
     }
-  }
-}
-
-// dS^T = P^T (dP^T - D), with P^T and dS^T packed to binary16 pairs: query
-// columns 2m, 2m+1 of the thread's half in [m].  With kMasked a column whose
-// P is 0 gets dS = 0 whatever its dP and D hold.
-template <bool kMasked>
-__device__ __forceinline__ void key_grads(const uint32_t (&sr)[64], const float *Ds,
-                                          uint32_t dp_taddr, uint32_t (&pp)[32],
-                                          uint32_t (&pd)[32]) {
-#pragma unroll
-  for (int c2 = 0; c2 < 2; ++c2) {
-    uint32_t dr[32];
-    tmem_ld_x32(dp_taddr + 32u * c2, dr);
-#pragma unroll
-    for (int t4 = 0; t4 < 8; ++t4) {
-      const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 32 * c2 + 4 * t4);
-      const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-      float pv[4], dv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pv[e] = __uint_as_float(sr[32 * c2 + 4 * t4 + e]);
-        const float g = pv[e] * (__uint_as_float(dr[4 * t4 + e]) - Dv[e]);
-        dv[e] = !kMasked || pv[e] != 0.f ? g : 0.f;
-      }
-      pp[16 * c2 + 2 * t4] = pack_half2(pv[0], pv[1]);
-      pp[16 * c2 + 2 * t4 + 1] = pack_half2(pv[2], pv[3]);
-      pd[16 * c2 + 2 * t4] = pack_half2(dv[0], dv[1]);
-      pd[16 * c2 + 2 * t4 + 1] = pack_half2(dv[2], dv[3]);
-    }
+    pp[2 * t4] = pack_half2(pv[0], pv[1]);
+    pp[2 * t4 + 1] = pack_half2(pv[2], pv[3]);
+    pd[2 * t4] = pack_half2(dv[0], dv[1]);
+    pd[2 * t4 + 1] = pack_half2(dv[2], dv[3]);
   }
 }
 
@@ -665,8 +631,8 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 230)) return;
       if (!sy.wait_warp(kBarSFull, pos & 1, 231)) return;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld_x64(tmem + lane_base + kColS + col0, sr);
+      uint32_t sr[64], dr[64];
+      tmem_ld_2x64(tmem + lane_base + kColS + col0, tmem + lane_base + kColDP + col0, sr, dr);
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarSFree));
@@ -680,27 +646,17 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       const bool masked = qt == w.kt || qt * kTile + kTile > p.T;
       const int lo = key - (qt * kTile + col0);
       const int hi = min(kTile, p.T - qt * kTile) - col0;
-      if (masked)
-        key_probs<true>(sr, Ls, c, lo, hi);
-      else
-        key_probs<false>(sr, Ls, c, lo, hi);
-      if (!sy.wait_warp(kBarDpFull, pos & 1, 232)) return;
-      tc_fence_after();
       uint32_t pp[32], pd[32];
       if (masked)
-        key_grads<true>(sr, Ds, tmem + lane_base + kColDP + col0, pp, pd);
+        key_step<true>(sr, dr, Ls, Ds, c, lo, hi, pp, pd);
       else
-        key_grads<false>(sr, Ds, tmem + lane_base + kColDP + col0, pp, pd);
-      tc_fence_before();
-      __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarDpFree));
+        key_step<false>(sr, dr, Ls, Ds, c, lo, hi, pp, pd);
       if (i > 0) {   // the previous step's products must be done before P^T, dS^T are overwritten
         if (!sy.wait_warp(kBarDvDone, (pos - 1) & 1, 233)) return;
         if (!sy.wait_warp(kBarDkDone, (pos - 1) & 1, 234)) return;
         tc_fence_after();
       }
-      tmem_st_x32(tmem + lane_base + kColP + 32u * half, pp);
-      tmem_st_x32(tmem + lane_base + kColDS + 32u * half, pd);
+      tmem_st_2x32(tmem + lane_base + kColP + 32u * half, tmem + lane_base + kColDS + 32u * half, pp, pd);
       tc_fence_before();
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarPFull));
@@ -750,8 +706,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sy.bar(kBarSFull), 1);
     mbar_init(sy.bar(kBarSFree), kComputeWarps);
-    mbar_init(sy.bar(kBarDpFull), 1);
-    mbar_init(sy.bar(kBarDpFree), kComputeWarps);
     mbar_init(sy.bar(kBarPFull), kComputeWarps);
     mbar_init(sy.bar(kBarDvDone), 1);
     mbar_init(sy.bar(kBarDkDone), 1);
