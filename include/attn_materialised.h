@@ -52,7 +52,8 @@ size_t attn_materialised_workspace_bytes(int T, int heads, int kv_heads);
  * attn_fwd_materialised -- the forward pass through materialised planes.
  *
  * q, k, vT, o, lse: device pointers, 16-byte aligned, layouts as attn_fwd.
- * T, heads, kv_heads, c: as attn_fwd (the same admission).
+ * T, heads, kv_heads, c: as attn_fwd (the same admission), and T <= 16384 (the
+ *   planes grow as heads * T^2).
  * workspace: device buffer of at least attn_materialised_workspace_bytes
  *   bytes, 256-byte aligned; its contents on entry do not matter.
  * stream: the stream to run on.

@@ -7,9 +7,11 @@
 // launch writing binary16 probabilities, then their product with V).  Three
 // launches:
 //   scores_kernel   S = Q K^T per (head, query tile, key tile <= diagonal): TMA
-//                   loads, four tcgen05 MMAs into tensor memory, binary32 rows out;
-//   softmax_kernel  one CTA per row: t = S c, row max, 2^(t - m), row sum,
-//                   normalised binary16 probabilities and the base-2 LSE;
+//                   loads, four tcgen05 MMAs into tensor memory, the binary32
+//                   tile staged in shared memory and written by TMA stores;
+//   softmax_kernel  one warp per row: t = S c, an online row maximum and sum in
+//                   one pass, then normalised binary16 probabilities and the
+//                   base-2 LSE;
 //   pv_kernel       O = P V per (head, query tile): a two-stage TMA ring of P and
 //                   V^T tiles, tcgen05 MMAs, binary16 O token-major.
 // Every wait is bounded (1 s); a timeout is recorded in a status word.
@@ -34,8 +36,7 @@ constexpr int kD = 64;
 constexpr int kTile = 128;
 constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KiB
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kMaxT = 16384;                      // a row of the scores plane stays in registers
-static_assert(kMaxT == 512 * 32, "the softmax kernel's largest register row");
+constexpr int kMaxT = 16384;                      // admission: the planes grow as T^2
 
 struct MatParams {
   int T, heads, kv_heads, group, q_tiles;
@@ -68,20 +69,24 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ---------------------------------------------------------------------------- scores
 // Block (kt, qt) of head h: grid.x enumerates the causal tiles (qt, kt <= qt).
-constexpr uint32_t kScoresSmem = 2 * kTileBytes + 64 + 1024;
-constexpr uint32_t kScoresSmemRequest = 48 * 1024;   // at most four CTAs per SM: 4 x 128 TMEM columns
-static_assert(kScoresSmem <= kScoresSmemRequest, "scores kernel shared memory");
+// Shared memory: the Q and K tiles, then the binary32 result staged as four
+// 32-column boxes of 128 rows (128-byte swizzle) for the TMA store.
+constexpr uint32_t kStageOff = 2 * kTileBytes;
+constexpr uint32_t kBoxBytes = kTile * 32 * 4;       // 16 KiB
+constexpr uint32_t kScoresBarOff = kStageOff + 4 * kBoxBytes;
+constexpr uint32_t kScoresSmem = kScoresBarOff + 64 + 1024;   // two CTAs per SM: 2 x 128 TMEM columns
 
 __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                      const __grid_constant__ CUtensorMap tmK,
+                                                     const __grid_constant__ CUtensorMap tmS,
                                                      const MatParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t smem = (raw + 1023u) & ~1023u;
   uint8_t *smem_gen = smem_raw + (smem - raw);
-  const uint32_t bar_full = smem + 2 * kTileBytes, bar_done = bar_full + 8;
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem_gen + 2 * kTileBytes + 16);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_gen + 2 * kTileBytes + 20);
+  const uint32_t bar_full = smem + kScoresBarOff, bar_done = bar_full + 8;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem_gen + kScoresBarOff + 16);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_gen + kScoresBarOff + 20);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int rem = blockIdx.x;
@@ -127,22 +132,34 @@ __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUt
   tc_fence_after();
   uint32_t sr[128];
   tmem_ld_x128(tmem + ((uint32_t)(32 * warp) << 16), sr);
+  // row r's 32-column slice b goes to box b, row r: its eight 16-byte chunks
+  // permuted by the 128-byte swizzle (chunk c at c ^ (r mod 8))
+  const int r = 32 * warp + lane;
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint32_t addr = smem + kStageOff + b * kBoxBytes + r * 128 + ((cc ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                   "r"(sr[32 * b + 4 * cc]), "r"(sr[32 * b + 4 * cc + 1]),
+                   "r"(sr[32 * b + 4 * cc + 2]), "r"(sr[32 * b + 4 * cc + 3])
+                   : "memory");
+    }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
-  if (!*abort_flag) {
-    const int row = qt * kTile + 32 * warp + lane;
-    const int cols = min(kTile, p.T - kt * kTile);   // 64 or 128
-    if (row < p.T) {
-      float4 *dst = reinterpret_cast<float4 *>(p.S + ((size_t)h * p.T + row) * p.T + kt * kTile);
+  if (threadIdx.x == 0) {
+    if (!*abort_flag) {
+      // rows past T are clipped by the copy; a 64-key last tile stores two boxes
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (4 * i < cols)
-          dst[i] = make_float4(__uint_as_float(sr[4 * i]), __uint_as_float(sr[4 * i + 1]),
-                               __uint_as_float(sr[4 * i + 2]), __uint_as_float(sr[4 * i + 3]));
+      for (int b = 0; b < 4; ++b)
+        if (kt * kTile + 32 * b < p.T)
+          tma_store_3d(&tmS, smem + kStageOff + b * kBoxBytes, kt * kTile + 32 * b, qt * kTile, h);
+      tma_store_commit_wait();
+    } else {
+      // let a copy that is still in flight land before the shared memory is released
+      wait_bounded(bar_full, 0, p.status, 303);
     }
-  } else if (threadIdx.x == 0) {
-    // let a copy that is still in flight land before the shared memory is released
-    wait_bounded(bar_full, 0, p.status, 303);
   }
   if (warp == 0) {
     tc_fence_after();
@@ -151,76 +168,64 @@ __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------------------- softmax
-// One CTA of 256 threads per (row i, head h).  Thread t holds the key pairs
-// (2(t + 256k), 2(t + 256k) + 1), k < kPairs, of the row in registers
-// (512 kPairs >= T).
-__device__ __forceinline__ float block_reduce(float x, bool is_max, float *red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float y = __shfl_xor_sync(0xffffffffu, x, off);
-    x = is_max ? fmaxf(x, y) : x + y;
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    x = lane < 8 ? red[lane] : (is_max ? -INFINITY : 0.f);
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) {
-      const float y = __shfl_xor_sync(0xffffffffu, x, off);
-      x = is_max ? fmaxf(x, y) : x + y;
-    }
-    if (lane == 0) red[8] = x;
-  }
-  __syncthreads();
-  const float r = red[8];
-  __syncthreads();   // red is reused by the next reduction
-  return r;
+// One warp per (row i, head h), eight rows per CTA.  Pass 1 streams the row's
+// causal scores once (a float4 per lane per step), keeping per lane a running
+// maximum m of t = S c and a sum l = sum 2^(t - m) rescaled whenever m rises;
+// the lanes' pairs are then merged.  Pass 2 reads the scores again (the row
+// was just read, so mostly from L2) and writes the normalised binary16
+// probabilities, zero-filled to the end of the diagonal tile.  (Holding the
+// row in registers instead, over four warps, measured slower: it halves the
+// rows in flight per SM.)
+__device__ __forceinline__ float rescale(float m_old, float m_new) {
+  return m_old == -INFINITY ? 0.f : ex2(m_old - m_new);
 }
 
-template <int kPairs>
 __global__ void __launch_bounds__(256) softmax_kernel(const MatParams p) {
-  __shared__ float red[9];
-  const int i = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp, h = blockIdx.y;
+  if (i >= p.T) return;
   const float *srow = p.S + ((size_t)h * p.T + i) * p.T;
   __half *prow = p.P + ((size_t)h * p.T + i) * p.T;
   const int n = i + 1;                                   // keys 0 .. i
   const int end = min(p.T, (i / kTile + 1) * kTile);     // the diagonal tile's end
   const float c = p.c;
-  float2 v[kPairs];
-  float mx = -INFINITY;
+  float m = -INFINITY, l = 0.f;
+#pragma unroll 4
+  for (int j0 = 4 * lane; j0 < n; j0 += 128) {
+    const float4 a = *reinterpret_cast<const float4 *>(srow + j0);
+    float t[4] = {a.x * c, a.y * c, a.z * c, a.w * c};
 #pragma unroll
-  for (int k = 0; k < kPairs; ++k) {
-    const int j = 2 * (t + 256 * k);
-    if (j < n) {
-      float2 a = *reinterpret_cast<const float2 *>(srow + j);
-      if (j + 1 >= n) a.y = -INFINITY;
-      v[k] = a;
-      mx = fmaxf(mx, fmaxf(a.x, a.y));
-    }
+    for (int e = 1; e < 4; ++e)
+      if (j0 + e >= n) t[e] = -INFINITY;
+    const float m_new = fmaxf(m, fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])));
+    l = l * rescale(m, m_new) + ((ex2(t[0] - m_new) + ex2(t[1] - m_new)) +
+                                 (ex2(t[2] - m_new) + ex2(t[3] - m_new)));
+    m = m_new;
   }
-  // t = S c is monotone in S for c > 0, so the row maximum of t is fl(max S * c)
-  const float m = block_reduce(mx, true, red) * c;
-  float l = 0.f;
 #pragma unroll
-  for (int k = 0; k < kPairs; ++k) {
-    const int j = 2 * (t + 256 * k);
-    if (j < n) {
-      const float p0 = ex2(fmaf(v[k].x, c, -m));
-      const float p1 = j + 1 < n ? ex2(fmaf(v[k].y, c, -m)) : 0.f;
-      v[k] = make_float2(p0, p1);
-      l += p0 + p1;
-    }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    const float m_new = fmaxf(m, m2);
+    l = l * rescale(m, m_new) + l2 * rescale(m2, m_new);
+    m = m_new;
   }
-  l = block_reduce(l, false, red);
   const float inv = 1.f / l;
-  if (t == 0) p.lse[(size_t)h * p.T + i] = m + log2f(l);
+  if (lane == 0) p.lse[(size_t)h * p.T + i] = m + log2f(l);
+#pragma unroll 4
+  for (int j0 = 4 * lane; j0 < end; j0 += 128) {
+    float q[4] = {0.f, 0.f, 0.f, 0.f};
+    if (j0 < n) {
+      const float4 a = *reinterpret_cast<const float4 *>(srow + j0);
+      const float t[4] = {a.x * c, a.y * c, a.z * c, a.w * c};
 #pragma unroll
-  for (int k = 0; k < kPairs; ++k) {
-    const int j = 2 * (t + 256 * k);
-    if (j < end)
-      *reinterpret_cast<__half2 *>(prow + j) =
-          j < n ? __floats2half2_rn(v[k].x * inv, v[k].y * inv) : __floats2half2_rn(0.f, 0.f);
+      for (int e = 0; e < 4; ++e) q[e] = j0 + e < n ? ex2(t[e] - m) * inv : 0.f;
+    }
+    __half2 lo = __floats2half2_rn(q[0], q[1]), hi = __floats2half2_rn(q[2], q[3]);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t *>(&lo);
+    v.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(prow + j0) = v;
   }
 }
 
@@ -370,7 +375,7 @@ int mat_state(MatState **out) {
       g_mat_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kScoresSmemRequest) != cudaSuccess ||
+                             (int)kScoresSmem) != cudaSuccess ||
         cudaFuncSetAttribute(pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPvSmem) != cudaSuccess)
       return ATTN_ELAUNCH;
@@ -383,12 +388,13 @@ int mat_state(MatState **out) {
 }
 
 bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-               uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1) {
+               uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {stride1, stride2};
   cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return g_mat_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+  return g_mat_encode(m, dtype, 3, const_cast<void *>(base), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -465,28 +471,18 @@ extern "C" int attn_fwd_materialised(const void *q, const void *k, const void *v
   p.status = st->status;
 
   const uint64_t rowb = kD * 2, trow = (uint64_t)T * 2;
-  CUtensorMap tmQ, tmK, tmP, tmVT;
+  CUtensorMap tmQ, tmK, tmP, tmVT, tmS;
   if (!encode_3d(&tmQ, q, kD, T, heads, rowb, rowb * T, kD, kTile) ||
+      !encode_3d(&tmS, p.S, T, T, heads, (uint64_t)T * 4, (uint64_t)T * T * 4, 32, kTile,
+                 CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
       !encode_3d(&tmK, k, kD, T, kv_heads, rowb, rowb * T, kD, kTile) ||
       !encode_3d(&tmP, p.P, T, T, heads, trow, trow * T, 64, kTile) ||
       !encode_3d(&tmVT, vT, T, kD, kv_heads, trow, trow * kD, 64, kD))
     return ATTN_ELAUNCH;
 
   const int tri = p.q_tiles * (p.q_tiles + 1) / 2;
-  scores_kernel<<<dim3(tri, heads), 128, kScoresSmemRequest, stream>>>(tmQ, tmK, p);
-  const dim3 sg(T, heads);
-  if (T <= 512)
-    softmax_kernel<1><<<sg, 256, 0, stream>>>(p);
-  else if (T <= 1024)
-    softmax_kernel<2><<<sg, 256, 0, stream>>>(p);
-  else if (T <= 2048)
-    softmax_kernel<4><<<sg, 256, 0, stream>>>(p);
-  else if (T <= 4096)
-    softmax_kernel<8><<<sg, 256, 0, stream>>>(p);
-  else if (T <= 8192)
-    softmax_kernel<16><<<sg, 256, 0, stream>>>(p);
-  else
-    softmax_kernel<32><<<sg, 256, 0, stream>>>(p);
+  scores_kernel<<<dim3(tri, heads), 128, kScoresSmem, stream>>>(tmQ, tmK, tmS, p);
+  softmax_kernel<<<dim3((T + 7) / 8, heads), 256, 0, stream>>>(p);
   pv_kernel<<<dim3(p.q_tiles, heads), 128, kPvSmem, stream>>>(tmP, tmVT, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;

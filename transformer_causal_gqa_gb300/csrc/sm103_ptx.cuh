@@ -76,6 +76,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
+// 3-D tiled tensor store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(tmap), "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// Commits this thread's bulk stores and waits until they are complete.
+__device__ __forceinline__ void tma_store_commit_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Allocates `ncols` TMEM columns (whole warp); the base address lands in smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
