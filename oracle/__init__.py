@@ -70,6 +70,10 @@ def open_library(path: str):
                                          i64p, i64p, i64, i64p, i64p, i64, f64p, f64p, f64p,
                                          ctypes.c_int]
     lib.oracle_attn_bwd_rows.restype = ctypes.c_int
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_qkv_rope.argtypes = [u16p, u16p, f32p, f32p, i64, i64, i64, i64, f64p, f64p, f64p,
+                                    ctypes.c_int]
+    lib.oracle_qkv_rope.restype = ctypes.c_int
     return lib
 
 
@@ -211,3 +215,29 @@ def attn_bwd_rows(q, k, vT, o, lse, dO, T: int, heads: int, kv_heads: int, c: fl
     if rc != 0:
         raise ValueError("oracle rejected the shape or an index")
     return dq, dk, dv
+
+
+def qkv_rope(x, w, cos_tab, sin_tab, T: int, width: int, heads: int, kv_heads: int,
+             threads: int = 0, lib=None):
+    """The fused QKV producer.  x: binary16 [T][width]; w: binary16
+    [(heads + 2 kv_heads) * 64][width] (parts Q, K, V); cos_tab, sin_tab: binary32
+    [T][32].  Returns (q [heads][T][64], k [kv_heads][T][64], vT [kv_heads][64][T]),
+    float64, unrounded."""
+    lib = lib or _load()
+    n_out = (heads + 2 * kv_heads) * HEAD_DIM
+    xb = _bits(x, (T, width))
+    wb = _bits(w, (n_out, width))
+    ct = np.ascontiguousarray(cos_tab, dtype=np.float32)
+    st = np.ascontiguousarray(sin_tab, dtype=np.float32)
+    if ct.shape != (T, HEAD_DIM // 2) or st.shape != (T, HEAD_DIM // 2):
+        raise ValueError("rotary tables must be [T][32] float32")
+    q = np.empty((heads, T, HEAD_DIM))
+    k = np.empty((kv_heads, T, HEAD_DIM))
+    vT = np.empty((kv_heads, HEAD_DIM, T))
+    rc = lib.oracle_qkv_rope(_ptr(xb, ctypes.c_uint16), _ptr(wb, ctypes.c_uint16),
+                             _ptr(ct, ctypes.c_float), _ptr(st, ctypes.c_float), T, width, heads,
+                             kv_heads, _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                             _ptr(vT, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the shape")
+    return q, k, vT

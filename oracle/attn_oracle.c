@@ -411,3 +411,68 @@ int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
     free(D);
     return 0;
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * The fused QKV producer (the launches that make Q, K and V^T for the forward
+ * pass): on the page ".../Coppelius/Build/Graph.alpha" a layer's attention
+ * inputs come from the QKV product of the normed activations with the QKV
+ * matrix (three parts), then "qk-rope" (rotary embedding of the query and key
+ * heads with the cosine and sine tables: a row per position, a column per
+ * head-dimension pair) and "value-transpose".  Written out, for token t:
+ *
+ *   y[t][n] = sum_i X[t][i] W[n][i]                  n < (heads + 2 kv_heads) * 64
+ *
+ * with the parts in the order Q (heads * 64 outputs), K (kv_heads * 64), V
+ * (kv_heads * 64) and head h of a part at its outputs h*64 .. h*64 + 63.  Query
+ * and key heads are rotated pair by pair: pair p of a head is its elements
+ * (2p, 2p + 1), and with c = C[t][p], s = S[t][p]
+ *
+ *   (a, b) -> (a c - b s,  a s + b c).
+ *
+ * Outputs (fp64, unrounded): q [heads][T][64], k [kv_heads][T][64],
+ * vT [kv_heads][64][T].  X and W are binary16 bit patterns, the tables
+ * binary32; all arithmetic is fp64.
+ */
+int oracle_qkv_rope(const uint16_t *x, const uint16_t *w, const float *cos_tab,
+                    const float *sin_tab, int64_t T, int64_t width, int64_t heads,
+                    int64_t kv_heads, double *q, double *k, double *vT, int threads)
+{
+    if (T <= 0 || width <= 0 || heads <= 0 || kv_heads <= 0 || heads % kv_heads != 0)
+        return -1;
+    half_table_init();
+    const int64_t n_out = (heads + 2 * kv_heads) * HEAD_DIM;
+    const int nt = resolve_threads(threads);
+    (void)nt;
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int64_t t = 0; t < T; ++t) {
+        double *y = (double *)malloc((size_t)n_out * sizeof(double));
+        const uint16_t *xr = x + t * width;
+        for (int64_t n = 0; n < n_out; ++n) {
+            const uint16_t *wr = w + n * width;
+            double acc = 0.0;
+            for (int64_t i = 0; i < width; ++i)
+                acc += g_half[xr[i]] * g_half[wr[i]];
+            y[n] = acc;
+        }
+        for (int64_t hh = 0; hh < heads + kv_heads; ++hh) {      /* query heads, then key heads */
+            const double *src = y + hh * HEAD_DIM;
+            double *dst = hh < heads ? q + (hh * T + t) * HEAD_DIM
+                                     : k + ((hh - heads) * T + t) * HEAD_DIM;
+            for (int p = 0; p < HEAD_DIM / 2; ++p) {
+                const double c = (double)cos_tab[t * (HEAD_DIM / 2) + p];
+                const double s = (double)sin_tab[t * (HEAD_DIM / 2) + p];
+                const double a = src[2 * p], b = src[2 * p + 1];
+                dst[2 * p] = a * c - b * s;
+                dst[2 * p + 1] = a * s + b * c;
+            }
+        }
+        for (int64_t g = 0; g < kv_heads; ++g) {                  /* value heads, transposed */
+            const double *src = y + (heads + kv_heads + g) * HEAD_DIM;
+            for (int e = 0; e < HEAD_DIM; ++e)
+                vT[(g * HEAD_DIM + e) * T + t] = src[e];
+        }
+        free(y);
+    }
+    return 0;
+}

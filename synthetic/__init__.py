@@ -15,7 +15,10 @@ Recipe (identical for both sides, which then read the same binary16 buffers):
   * V transposed per K/V head to V^T [kv_heads][64][T].
 For the backward pass the output gradient dO [T][heads*64] (O's token-major
 layout) is drawn from its own Philox stream, keyed by the seed plus
-0x9E3779B9, as standard-normal float32 rounded to binary16.
+0x9E3779B9, as standard-normal float32 rounded to binary16.  For the fused
+QKV producer, X and W come from a stream keyed by the seed plus 0x51ED2700,
+and the rotary tables are the nearest binary32 values of cos and sin of
+t * 10000^(-p/32).
 The scale constant c is the binary32 value nearest 0.125 / ln 2 (the head
 width 64 gives the score scale 1/sqrt(64) = 0.125).
 """
@@ -111,3 +114,29 @@ def make_output_grad(w: Workload):
     rng = np.random.Generator(np.random.Philox(w.seed + GRAD_SEED_OFFSET))
     g = rng.standard_normal((w.T, w.heads * HEAD_DIM), dtype=np.float32)
     return g.astype(np.float16)
+
+
+ROPE_BASE = 10000.0
+PRODUCER_SEED_OFFSET = 0x51ED2700
+
+
+def rotary_tables(T: int):
+    """cos and sin tables [T][32] as binary32: column p holds position t times
+    theta_p = 10000^(-p/32), evaluated in float64 and rounded once (the table is an
+    input of the producer, made here as the nearest binary32 values)."""
+    p = np.arange(HEAD_DIM // 2, dtype=np.float64)
+    theta = ROPE_BASE ** (-p / (HEAD_DIM // 2))
+    ang = np.arange(T, dtype=np.float64)[:, None] * theta[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def make_producer_inputs(T: int, width: int, heads: int, kv_heads: int, seed: int):
+    """Inputs of the fused QKV producer from their own Philox stream: X [T][width]
+    ~ N(0, 1) and W [(heads + 2 kv_heads) * 64][width] ~ N(0, 1/width), both
+    rounded to binary16, and the rotary tables."""
+    rng = np.random.Generator(np.random.Philox(seed + PRODUCER_SEED_OFFSET))
+    x = rng.standard_normal((T, width), dtype=np.float32)
+    n_out = (heads + 2 * kv_heads) * HEAD_DIM
+    w = rng.standard_normal((n_out, width), dtype=np.float32) * np.float32(1.0 / np.sqrt(width))
+    cos_t, sin_t = rotary_tables(T)
+    return x.astype(np.float16), w.astype(np.float16), cos_t, sin_t
