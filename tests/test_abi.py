@@ -194,3 +194,31 @@ def test_mat_workspace_bytes(lib):
     assert tcg.attn_materialised_workspace_bytes(1024, 12, 12) == 12 * 1024 * 1024 * 6
     assert tcg.attn_materialised_workspace_bytes(16384, 1, 1) == 16384 * 16384 * 6
     assert tcg.attn_materialised_workspace_bytes(16384 + 64, 1, 1) == 0
+
+
+# ---------------------------------------------------------------------------- producer entry
+def qkv_call(lib, T=128, width=128, H=4, G=2, **ptr):
+    """attn_qkv_rope with fake, well-separated device addresses (no launch happens on a
+    rejected call).  At T=128, width=128, H=4, G=2: x 32 KiB, w 64 KiB, tables 16 KiB each,
+    q 64 KiB, k and vT 32 KiB."""
+    base = dict(x=0x100000, w=0x200000, c=0x300000, s=0x400000, q=0x500000, k=0x600000,
+                v=0x700000)
+    base.update(ptr)
+    vp = ctypes.c_void_p
+    return lib.attn_qkv_rope(vp(base["x"]), vp(base["w"]), vp(base["c"]), vp(base["s"]),
+                             vp(base["q"]), vp(base["k"]), vp(base["v"]), T, width, H, G, None)
+
+
+@pytest.mark.parametrize("T,width,H,G", [
+    (0, 128, 4, 2), (100, 128, 4, 2), (128, 0, 4, 2), (128, 96, 4, 2), (128, 128, 4, 3),
+    (128, 128, 65536, 1), (2 ** 24, 64, 1, 1),
+])
+def test_qkv_rejects_inadmissible_shapes(lib, T, width, H, G):
+    assert qkv_call(lib, T=T, width=width, H=H, G=G) == tcg.ATTN_EINVAL
+
+
+def test_qkv_rejects_bad_pointers(lib):
+    assert qkv_call(lib, w=0) == tcg.ATTN_EINVAL
+    assert qkv_call(lib, c=0x300008) == tcg.ATTN_EALIGN
+    assert qkv_call(lib, q=0x100000 + 32768 - 16) == tcg.ATTN_EOVERLAP     # q over x
+    assert qkv_call(lib, v=0x600000 + 16) == tcg.ATTN_EOVERLAP             # vT over k

@@ -2,7 +2,8 @@
 streaming normalised sum, and its backward pass.
 
 A thin ctypes binding over the C ABI declared in ``include/attn_fwd.h`` and
-``include/attn_bwd.h`` and ``include/attn_materialised.h`` (``libattn_gb300.so``): it checks tensor dtypes,
+``include/attn_bwd.h``, ``include/attn_materialised.h`` and ``include/attn_qkv.h``
+(``libattn_gb300.so``): it checks tensor dtypes,
 devices and contiguity, and passes raw pointers, sizes and the stream handle.
 Every step of both passes runs in the library's CUDA kernels; there is no CPU
 path.  If the library has not been built, every entry point raises
@@ -37,7 +38,8 @@ EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
             "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
             "attn_bwd_last_device_status", "attn_bwd_test_inject_stall", "attn_fwd_materialised",
-            "attn_materialised_workspace_bytes", "attn_materialised_last_device_status")
+            "attn_materialised_workspace_bytes", "attn_materialised_last_device_status",
+            "attn_qkv_rope", "attn_qkv_last_device_status")
 
 _lib = None
 
@@ -91,6 +93,10 @@ def load_library():
     lib.attn_materialised_workspace_bytes.restype = sz
     lib.attn_materialised_last_device_status.argtypes = [vp]
     lib.attn_materialised_last_device_status.restype = i
+    lib.attn_qkv_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
+    lib.attn_qkv_rope.restype = i
+    lib.attn_qkv_last_device_status.argtypes = [vp]
+    lib.attn_qkv_last_device_status.restype = i
     _lib = lib
     return lib
 
@@ -280,3 +286,41 @@ def attn_fwd_materialised(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c
 def materialised_last_device_status(stream=None) -> int:
     """Synchronises ``stream``; ATTN_OK, or ATTN_ETIMEOUT if a materialised-path wait gave up."""
     return int(load_library().attn_materialised_last_device_status(_stream_handle(stream)))
+
+
+def attn_qkv_rope(x, w, cosines, sines, q, k, vT, T: int, width: int, heads: int,
+                  kv_heads: int, stream=None) -> None:
+    """The fused QKV producer on CUDA tensors: x binary16 [T][width], w binary16
+    [(heads + 2 kv_heads) * 64][width], cosines/sines binary32 [T][32]; writes
+    q [heads][T][64], k [kv_heads][T][64], vT [kv_heads][64][T] (binary16)."""
+    import torch
+    n_out = (heads + 2 * kv_heads) * HEAD_DIM
+    _check_tensor("x", x, torch.float16, (T, width))
+    _check_tensor("w", w, torch.float16, (n_out, width))
+    _check_tensor("cosines", cosines, torch.float32, (T, HEAD_DIM // 2))
+    _check_tensor("sines", sines, torch.float32, (T, HEAD_DIM // 2))
+    _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
+    _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))
+    _check_tensor("vT", vT, torch.float16, (kv_heads, HEAD_DIM, T))
+    rc = load_library().attn_qkv_rope(x.data_ptr(), w.data_ptr(), cosines.data_ptr(),
+                                      sines.data_ptr(), q.data_ptr(), k.data_ptr(), vT.data_ptr(),
+                                      int(T), int(width), int(heads), int(kv_heads),
+                                      _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_qkv_rope")
+
+
+def qkv_last_device_status(stream=None) -> int:
+    """Synchronises ``stream``; ATTN_OK, or ATTN_ETIMEOUT if a producer wait gave up."""
+    return int(load_library().attn_qkv_last_device_status(_stream_handle(stream)))
+
+
+def qkv_rope(x, w, cosines, sines, heads: int, kv_heads: int, stream=None):
+    """Allocates the outputs with torch and runs attn_qkv_rope; returns (q, k, vT)."""
+    import torch
+    T, width = x.shape
+    q = torch.empty((heads, T, HEAD_DIM), dtype=torch.float16, device=x.device)
+    k = torch.empty((kv_heads, T, HEAD_DIM), dtype=torch.float16, device=x.device)
+    vT = torch.empty((kv_heads, HEAD_DIM, T), dtype=torch.float16, device=x.device)
+    attn_qkv_rope(x, w, cosines, sines, q, k, vT, T, width, heads, kv_heads, stream)
+    return q, k, vT
