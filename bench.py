@@ -20,6 +20,12 @@ call per step: the same forward through a binary32 scores plane and a
 binary16 probability plane (three launches), reported in the same causal
 TFLOP/s and against the HBM roofline, since it moves the planes through memory.
 
+The producer mode (--pass producer) times one attn_qkv_rope call per step:
+the fused QKV product of the workload's tokens (width = heads * 64, the
+model's width) with a QKV matrix of heads + 2 kv_heads heads, rotary
+embedding and value transpose in its epilogue; it counts
+2 * T * width * (heads + 2 kv_heads) * 64 FLOPs against the tensor roofline.
+
 The backward mode times one attn_bwd call per step (the query launch and the
 key launch) on the same workload, with O and LSE from one forward pass made
 before timing and dO from the seeded generator; it counts the five products
@@ -55,6 +61,7 @@ import synthetic  # noqa: E402
 METRIC = "causal attn fwd TFLOP/s and % of GB300 dense fp16 tensor peak, T=8192"
 METRIC_BWD = "causal attn bwd TFLOP/s (five products) and % of GB300 dense fp16 tensor peak"
 METRIC_MAT = "materialised causal attn fwd TFLOP/s (scores + probability planes), HBM roofline"
+METRIC_QKV = "fused QKV producer (product + rotary + V transpose) TFLOP/s and % of fp16 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 512 << 20
@@ -62,6 +69,8 @@ KERNEL_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_t8192_h32_kv8.md")
 BWD_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_bwd.cu")
 BWD_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_bwd_t8192_h32_kv8.md")
+QKV_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_qkv.cu")
+QKV_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qkv_kernel_t8192_w2048_h32_kv8.md")
 
 
 def parse_args():
@@ -73,8 +82,8 @@ def parse_args():
     ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="which", choices=["forward", "backward", "materialised"],
-                    default="forward")
+    ap.add_argument("--pass", dest="which",
+                    choices=["forward", "backward", "materialised", "producer"], default="forward")
     return ap.parse_args()
 
 
@@ -775,9 +784,204 @@ def run_gb300_materialised(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- QKV producer
+def producer_shape(w):
+    width = w.heads * 64
+    n_out = (w.heads + 2 * w.kv_heads) * 64
+    return width, n_out, 2.0 * w.T * width * n_out
+
+
+def oracle_producer_sample(w, x, wt, c, s, n_tok):
+    """The oracle producer on the first n_tok tokens (every token costs the same)."""
+    import oracle
+    width, n_out, _ = producer_shape(w)
+    t0 = time.perf_counter()
+    oracle.qkv_rope(x[:n_tok], wt, c[:n_tok], s[:n_tok], n_tok, width, w.heads, w.kv_heads)
+    return time.perf_counter() - t0, 2.0 * n_tok * width * n_out
+
+
+def producer_calibrate(w, x, wt, c, s, target_s):
+    n = 8
+    while True:
+        dt, _ = oracle_producer_sample(w, x, wt, c, s, n)
+        if dt > 0.5 or n >= w.T:
+            break
+        n = min(w.T, n * 4)
+    return max(1, min(w.T, int(n * target_s / max(dt, 1e-6))))
+
+
+def run_gb300_producer(args):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        tcg_build.build()
+    if world > 1:
+        dist.barrier()
+    tcg.load_library()
+    base = synthetic.WORKLOADS[args.workload]
+    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    T, H, G = w.T, w.heads, w.kv_heads
+    width, n_out, flops = producer_shape(w)
+    host = synthetic.make_producer_inputs(T, width, H, G, w.seed)
+    xd, wd, cd, sd = (torch.from_numpy(a).to(dev) for a in host)
+    q = torch.empty((H, T, 64), dtype=torch.float16, device=dev)
+    k = torch.empty((G, T, 64), dtype=torch.float16, device=dev)
+    vT = torch.empty((G, 64, T), dtype=torch.float16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tcg.attn_qkv_rope(xd, wd, cd, sd, q, k, vT, T, width, H, G, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    if tcg.qkv_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("producer device status after warm-up is not OK")
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid())
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if tcg.qkv_last_device_status(stream) != tcg.ATTN_OK:
+        raise RuntimeError("producer device status after the timed steps is not OK")
+    per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    dev_s = sum(per_ms) / 1e3
+
+    hin = [torch.from_numpy(a).pin_memory() for a in host]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, vT)]
+    din = [torch.empty_like(t) for t in (xd, wd, cd, sd)]
+
+    def e2e_step():
+        for d, h in zip(din, hin):
+            d.copy_(h, non_blocking=True)
+        tcg.attn_qkv_rope(*din, q, k, vT, T, width, H, G, stream)
+        for h, d in zip(hout, (q, k, vT)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+        stream.synchronize()
+    E = max(1, args.e2e_steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - e0
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    if rank == 0:
+        avg_s = statistics.fmean(per_ms) / 1e3
+        peak, peak_note = measured_peak()
+        achieved = flops / avg_s / 1e12
+        cfg = dict(workload_config(w, "flushed between timed steps (512 MiB write); each launch "
+                                      "timed by CUDA events"),
+                   **{"pass": "producer"}, width=width, outputs=n_out, flops_per_step=flops,
+                   inputs_producer="X ~ N(0,1), W ~ N(0,1/width) binary16 (Philox); rotary "
+                                   "tables cos/sin(t * 10000^(-p/32)) binary32",
+                   parallelism=f"independent problem per GPU x{world}")
+        cfg.pop("causal_flops_per_step", None)
+        line = {
+            "metric": METRIC_QKV, "value": world * K * flops / dev_s / 1e12, "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+            "ms_per_step": dev_s / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak,
+                         "traffic": kernel_traffic(QKV_TRAFFIC_SUMMARY, QKV_SOURCE),
+                         "peak_source": peak_note, "kernel": "qkv_kernel",
+                         "launch_ms": {"mean": avg_s * 1e3, "median": statistics.median(per_ms),
+                                       "min": min(per_ms)}},
+            "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "attn_qkv_rope binding: pinned host inputs copied in, the call, "
+                            "Q, K, V^T copied out, synchronised each step"},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            import oracle
+            n = producer_calibrate(base, *host, 15.0)
+            dt, fl = oracle_producer_sample(base, *host, n)
+            line["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+                "kind": "oracle",
+                "sample": f"the first {n} of {T} tokens (every token costs the same; fp64 "
+                          f"oracle, {dt:.1f} s)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_producer(args):
+    import oracle
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    width, n_out, _ = producer_shape(w)
+    host = synthetic.make_producer_inputs(w.T, width, w.heads, w.kv_heads, w.seed)
+    K, W = max(1, args.steps), max(3, args.warmup)
+    n = producer_calibrate(w, *host, 120.0 / (K + W))
+    for _ in range(W):
+        oracle_producer_sample(w, *host, n)
+    tot_s = tot_fl = 0.0
+    for _ in range(K):
+        dt, fl = oracle_producer_sample(w, *host, n)
+        tot_s += dt
+        tot_fl += fl
+    value = tot_fl / tot_s / 1e12
+    cfg = dict(workload_config(w, "not applicable (host CPU)"), **{"pass": "producer"},
+               width=width, outputs=n_out, parallelism="host cores of rank 0")
+    cfg.pop("causal_flops_per_step", None)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_QKV, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": tot_s / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"each step: the first {n} tokens"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.which == "materialised":
+    if args.which == "producer":
+        (run_reference_producer if args.impl == "reference" else run_gb300_producer)(args)
+    elif args.which == "materialised":
         if args.impl == "reference":
             run_reference(args, metric=METRIC_MAT)
         else:

@@ -4,10 +4,11 @@
 // transpose done in the product's epilogue (the page ".../Coppelius/Build/Graph.alpha"
 // runs these as the QKV product, then "qk-rope", then "value-transpose").
 //
-// One persistent CTA per SM walks output tiles of 128 tokens x 256 outputs
-// (four heads).  Warp 0 (one lane) streams 64-wide slices of the X and W
-// tiles through a four-stage TMA ring; warp 1 issues the tcgen05 MMAs
-// (M = 128, N = 256, K = 16) into one of two tensor-memory accumulators;
+// One persistent CTA per SM walks output tiles of 128 tokens x 192 outputs
+// (three heads: 1024 tiles fill seven waves of 152 SMs to 96 %, where four-head
+// tiles filled six to 84 %).  Warp 0 (one lane) streams 64-wide slices of the
+// X and W tiles through a five-stage TMA ring; warp 1 issues the tcgen05 MMAs
+// (M = 128, N = 192, K = 16) into one of two tensor-memory accumulators;
 // warps 2-5 (one token per thread) take a finished accumulator, rotate the
 // query and key heads' pairs in binary32, round to binary16 and write Q and K
 // rows and V^T columns, while the next tile accumulates in the other buffer.
@@ -31,11 +32,11 @@ using namespace sm103;
 
 constexpr int kD = 64;                      // head width
 constexpr int kBM = 128;                    // tokens per tile (= TMEM lanes)
-constexpr int kBN = 256;                    // outputs per tile: four heads
+constexpr int kBN = 192;                    // outputs per tile: three heads
 constexpr int kBK = 64;                     // width slice per stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KiB
-constexpr uint32_t kBBytes = kBN * kBK * 2;   // 32 KiB
+constexpr uint32_t kBBytes = kBN * kBK * 2;   // 24 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kOffBar = kStages * kStageBytes;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages,
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem + kOffTmemPtr, 2 * kBN);
+    tmem_alloc(smem + kOffTmemPtr, 512);   // two accumulators of kBN columns
     tmem_relinquish();
   }
   tc_fence_before();
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kBN);
+    tmem_dealloc(tmem, 512);
   }
 }
 
