@@ -82,6 +82,8 @@ def parse_args():
     ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=120.0,
+                    help="CPU seconds the reference arm spends over warm-up and timed steps")
     ap.add_argument("--pass", dest="which",
                     choices=["forward", "backward", "materialised", "producer"], default="forward")
     return ap.parse_args()
@@ -90,6 +92,22 @@ def parse_args():
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def rank_problem(base, rank):
+    """The workload each rank runs: the same shape, its own seed (an independent problem)."""
+    return dataclasses.replace(base, seed=base.seed + 7919 * rank)
+
+
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets the
+    step time); the values themselves when world == 1."""
+    import torch
+    import torch.distributed as dist
+    vals = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    return [float(x) for x in vals.tolist()]
 
 
 def workload_config(w, l2_note):
@@ -258,7 +276,7 @@ def run_gb300(args):
     tcg.load_library()
 
     base = synthetic.WORKLOADS[args.workload]
-    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)   # an independent problem per rank
+    w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     c = synthetic.scale_c()
     q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
@@ -324,10 +342,7 @@ def run_gb300(args):
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
-    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    dev_s, e2e_s, wall = max_over_ranks([dev_s, e2e_s, wall], dev, world)
 
     if rank == 0:
         flops = w.causal_flops
@@ -375,7 +390,7 @@ def run_reference(args, metric=METRIC):
     w = synthetic.WORKLOADS[args.workload]
     inputs = synthetic.make_inputs(w)
     K, W = max(1, args.steps), max(3, args.warmup)
-    budget_s = 120.0
+    budget_s = args.reference_budget_s
     rows = calibrate_rows(w, inputs, budget_s / (K + W))
     for i in range(W):
         oracle_sample(w, inputs, rows, seed=100 + i)
@@ -462,7 +477,7 @@ def run_gb300_backward(args):
     tcg.load_library()
 
     base = synthetic.WORKLOADS[args.workload]
-    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     dO_np = synthetic.make_output_grad(w)
     c, s_nat = synthetic.scale_c(), 0.125
@@ -539,10 +554,7 @@ def run_gb300_backward(args):
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
 
-    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    dev_s, e2e_s, wall = max_over_ranks([dev_s, e2e_s, wall], dev, world)
     if rank == 0:
         flops = bwd_flops(w)
         avg_s = statistics.fmean(per_call_ms) / 1e3
@@ -602,7 +614,7 @@ def run_reference_backward(args):
     dO = synthetic.make_output_grad(w)
     o, lse = bwd_oracle_inputs(w, inputs)
     K, W = max(1, args.steps), max(3, args.warmup)
-    n = bwd_calibrate(w, inputs, o, lse, dO, 120.0 / (K + W))
+    n = bwd_calibrate(w, inputs, o, lse, dO, args.reference_budget_s / (K + W))
     for i in range(W):
         oracle_bwd_sample(w, inputs, o, lse, dO, n, seed=100 + i)
     tot_s = tot_fl = 0.0
@@ -672,7 +684,7 @@ def run_gb300_materialised(args):
         dist.barrier()
     tcg.load_library()
     base = synthetic.WORKLOADS[args.workload]
-    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     c = synthetic.scale_c()
     T, H, G = w.T, w.heads, w.kv_heads
@@ -743,10 +755,7 @@ def run_gb300_materialised(args):
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
-    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    dev_s, e2e_s, wall = max_over_ranks([dev_s, e2e_s, wall], dev, world)
     if rank == 0:
         flops = w.causal_flops
         avg_s = statistics.fmean(per_call_ms) / 1e3
@@ -828,7 +837,7 @@ def run_gb300_producer(args):
         dist.barrier()
     tcg.load_library()
     base = synthetic.WORKLOADS[args.workload]
-    w = dataclasses.replace(base, seed=base.seed + 7919 * rank)
+    w = rank_problem(base, rank)
     T, H, G = w.T, w.heads, w.kv_heads
     width, n_out, flops = producer_shape(w)
     host = synthetic.make_producer_inputs(T, width, H, G, w.seed)
@@ -897,10 +906,7 @@ def run_gb300_producer(args):
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = sum(t.numel() * t.element_size() for t in hout)
 
-    vals = torch.tensor([dev_s, e2e_s, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    dev_s, e2e_s, wall = (float(x) for x in vals.tolist())
+    dev_s, e2e_s, wall = max_over_ranks([dev_s, e2e_s, wall], dev, world)
     if rank == 0:
         avg_s = statistics.fmean(per_ms) / 1e3
         peak, peak_note = measured_peak()
@@ -954,7 +960,7 @@ def run_reference_producer(args):
     width, n_out, _ = producer_shape(w)
     host = synthetic.make_producer_inputs(w.T, width, w.heads, w.kv_heads, w.seed)
     K, W = max(1, args.steps), max(3, args.warmup)
-    n = producer_calibrate(w, *host, 120.0 / (K + W))
+    n = producer_calibrate(w, *host, args.reference_budget_s / (K + W))
     for _ in range(W):
         oracle_producer_sample(w, *host, n)
     tot_s = tot_fl = 0.0
