@@ -76,3 +76,8 @@ def test_deterministic():
     b = run(512, 256, 8, 2, seed=9)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_headline_size_every_element():
+    # the benchmark's shape: 8192 tokens, width 2048, 32 query heads over 8 K/V heads
+    run(8192, 2048, 32, 8, seed=synthetic.WORKLOADS[synthetic.HEADLINE].seed)
