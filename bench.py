@@ -368,8 +368,9 @@ def run_gb300(args):
                                        "min": min(per_launch_ms)}},
             "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "attn_fwd_host: pinned host buffers, copies + kernel on one stream, "
-                            "synchronised each step"},
+                    "path": "attn_fwd_host: pinned host buffers; four K/V-head chunks, copies in "
+                            "and out on two library streams overlapping the kernel on the "
+                            "caller's stream; synchronised each step"},
             "gpu_launches": K,
             "clocks": clocks,
             "wall_s_timed_region": wall,

@@ -89,11 +89,17 @@ size_t attn_fwd_workspace_bytes(int T, int heads, int kv_heads);
 
 /*
  * attn_fwd_host -- the forward pass on HOST buffers (same layouts as
- * attn_fwd).  Queues on `stream`: copies of q, k, vT into `workspace` (a
- * device buffer of at least attn_fwd_workspace_bytes bytes, 256-byte aligned,
- * owned by the caller), the kernel, and copies of O and LSE back into o and
- * lse.  Host buffers should be page-locked for the copies to be asynchronous;
- * the caller synchronises `stream` before reading o and lse.
+ * attn_fwd).  The problem is cut into up to four groups of K/V heads (with
+ * their query heads); for each group the call queues the copies of its q, k,
+ * vT slices into `workspace` (a device buffer of at least
+ * attn_fwd_workspace_bytes bytes, 256-byte aligned, owned by the caller), the
+ * kernel on `stream`, and the copies of its O columns and LSE rows back into
+ * o and lse.  The copies in and out run on two streams the library creates
+ * once per device, ordered by events after the work already queued on
+ * `stream`, so both directions overlap the compute; `stream` completes only
+ * after the last copy out.  Host buffers should be page-locked for the copies
+ * to be asynchronous; the caller synchronises `stream` before reading o and
+ * lse.  Calls from several host threads are serialised while they queue.
  * Errors as attn_fwd; ATTN_EINVAL also if workspace_bytes is too small.
  */
 int attn_fwd_host(const void *q, const void *k, const void *vT, void *o, float *lse,

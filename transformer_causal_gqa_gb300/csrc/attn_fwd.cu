@@ -745,6 +745,47 @@ extern "C" size_t attn_fwd_workspace_bytes(int T, int heads, int kv_heads) {
   return up(z.q) + 2 * up(z.kv) + up(z.o) + up(z.lse);
 }
 
+namespace {
+// attn_fwd_host's pipeline: the problem is cut into up to kHostChunks groups of
+// K/V heads; chunk c's inputs are copied in on one stream while the kernel runs
+// on chunk c - 1 on the caller's stream and chunk c - 2's outputs are copied out
+// on a third, so the transfers in both directions overlap the compute.
+constexpr int kHostChunks = 4;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_done[kHostChunks] = {}, comp_done[kHostChunks] = {};
+};
+std::mutex g_pipe_mutex;
+HostPipe g_pipe[64];
+
+int host_pipe(HostPipe **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return ATTN_EDEVICE;
+  }
+  HostPipe &hp = g_pipe[dev];
+  if (!hp.ready) {
+    bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kHostChunks; ++i)
+      ok = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.comp_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return ATTN_ELAUNCH;
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return ATTN_OK;
+}
+}  // namespace
+
 extern "C" int attn_fwd_host(const void *q, const void *k, const void *vT, void *o, float *lse,
                              int T, int heads, int kv_heads, float c, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
@@ -753,21 +794,58 @@ extern "C" int attn_fwd_host(const void *q, const void *k, const void *vT, void 
   if (!q || !k || !vT || !o || !lse || !workspace) return ATTN_EINVAL;
   if (workspace_bytes < attn_fwd_workspace_bytes(T, heads, kv_heads)) return ATTN_EINVAL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_EALIGN;
+  DeviceState *st = nullptr;
+  if ((rc = device_state(&st))) return rc;   // before the pipeline: reports a missing device
   const Sizes z = sizes_of(T, heads, kv_heads);
   auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   uint8_t *dq = ws, *dk = dq + up(z.q), *dv = dk + up(z.kv), *dout = dv + up(z.kv),
           *dlse = dout + up(z.o);
-  if (cudaMemcpyAsync(dq, q, z.q, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k, z.kv, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dv, vT, z.kv, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ELAUNCH;
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);   // one call's events at a time
+  HostPipe *hp = nullptr;
+  if ((rc = host_pipe(&hp))) return rc;
+  const int group = heads / kv_heads;
+  const int chunks = kv_heads < kHostChunks ? kv_heads : kHostChunks;
+  const size_t head_bytes = (size_t)T * kHeadDim * 2;   // one head of Q, K or V^T
+  bool ok = cudaEventRecord(hp->start, stream) == cudaSuccess &&
+            cudaStreamWaitEvent(hp->in, hp->start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(hp->out, hp->start, 0) == cudaSuccess;
+  size_t o_off = 0;   // chunk c's O, [T][its heads x 64], lies whole in the device O region
+  for (int ch = 0; ok && ch < chunks; ++ch) {
+    const int g0 = (int)((long long)kv_heads * ch / chunks);
+    const int g1 = (int)((long long)kv_heads * (ch + 1) / chunks);
+    const int h0 = g0 * group, hc = (g1 - g0) * group;
+    const uint8_t *hq = static_cast<const uint8_t *>(q) + (size_t)h0 * head_bytes;
+    const uint8_t *hk = static_cast<const uint8_t *>(k) + (size_t)g0 * head_bytes;
+    const uint8_t *hv = static_cast<const uint8_t *>(vT) + (size_t)g0 * head_bytes;
+    uint8_t *cq = dq + (size_t)h0 * head_bytes, *ck = dk + (size_t)g0 * head_bytes,
+            *cv = dv + (size_t)g0 * head_bytes, *co = dout + o_off;
+    float *clse = reinterpret_cast<float *>(dlse) + (size_t)h0 * T;
+    ok = cudaMemcpyAsync(cq, hq, (size_t)hc * head_bytes, cudaMemcpyHostToDevice, hp->in) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(ck, hk, (size_t)(g1 - g0) * head_bytes, cudaMemcpyHostToDevice, hp->in) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(cv, hv, (size_t)(g1 - g0) * head_bytes, cudaMemcpyHostToDevice, hp->in) ==
+             cudaSuccess &&
+         cudaEventRecord(hp->in_done[ch], hp->in) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, hp->in_done[ch], 0) == cudaSuccess;
+    if (!ok) break;
+    if ((rc = attn_fwd(cq, ck, cv, co, clse, T, hc, g1 - g0, c, stream))) return rc;
+    // O's chunk is a column block of the host's [T][heads x 64]: a 2-D copy
+    ok = cudaEventRecord(hp->comp_done[ch], stream) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->out, hp->comp_done[ch], 0) == cudaSuccess &&
+         cudaMemcpy2DAsync(static_cast<uint8_t *>(o) + (size_t)h0 * kHeadDim * 2,
+                           (size_t)heads * kHeadDim * 2, co, (size_t)hc * kHeadDim * 2,
+                           (size_t)hc * kHeadDim * 2, T, cudaMemcpyDeviceToHost, hp->out) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(lse + (size_t)h0 * T, clse, (size_t)hc * T * 4, cudaMemcpyDeviceToHost,
+                         hp->out) == cudaSuccess;
+    o_off += (size_t)hc * head_bytes;
   }
-  rc = attn_fwd(dq, dk, dv, dout, reinterpret_cast<float *>(dlse), T, heads, kv_heads, c, stream);
-  if (rc) return rc;
-  if (cudaMemcpyAsync(o, dout, z.o, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaMemcpyAsync(lse, dlse, z.lse, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+  // the caller's stream completes only after the last copy out
+  ok = ok && cudaEventRecord(hp->done, hp->out) == cudaSuccess &&
+       cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess;
+  if (!ok) {
     cudaGetLastError();
     return ATTN_ELAUNCH;
   }
