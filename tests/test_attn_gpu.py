@@ -120,8 +120,11 @@ def test_deterministic_and_stream():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_host_entry_matches_device_entry():
-    w = synthetic.custom(640, 8, 4, seed=81)
+# the host entry cuts the problem into up to four K/V-head chunks: one chunk,
+# one head per chunk, uneven chunks (6 -> 1, 2, 1, 2; 12 -> 3 each) and MHA
+@pytest.mark.parametrize("H,G", [(8, 4), (4, 1), (12, 6), (24, 12), (16, 16)])
+def test_host_entry_matches_device_entry(H, G):
+    w = synthetic.custom(640, H, G, seed=81 + H)
     q, k, vT = synthetic.make_inputs(w)
     c = synthetic.scale_c()
     o_dev, lse_dev = run_gpu(q, k, vT, w.T, w.heads, w.kv_heads, c)
