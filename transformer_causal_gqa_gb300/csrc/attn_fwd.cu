@@ -11,19 +11,29 @@
 // visited, and only the diagonal tile is masked (key column > query row).
 //
 // How (GB300-first, not the page's SM86 register-fragment design):
-//   * a persistent grid, one CTA per SM, walks work units of 256 query rows
-//     of one head (two 128-row subtiles sharing every K/V^T tile), heaviest
-//     (latest) row blocks first in a serpentine order across the CTAs;
+//   * a persistent grid, one CTA per SM, takes work units of 256 query rows
+//     of one head (two 128-row subtiles sharing every K/V^T tile) from a
+//     global counter, heaviest (latest) row blocks first;
 //   * one warp issues TMA loads: Q subtiles and a ring of 16 KiB K and V^T
 //     tiles (128 keys x 64), 128-byte swizzled, signalled by mbarriers;
-//   * one thread issues tcgen05 MMAs: S = Q K^T (M=128, N=128, K=64) into
-//     tensor memory, then O += P V (M=128, N=64, K=128) with P read from
-//     tensor memory where the softmax wrote it over S;
+//   * three warps issue tcgen05 MMAs: one issues S = Q K^T (M=128, N=128,
+//     K=64) into tensor memory for both subtiles, in whichever order their S
+//     buffers free up; one per subtile issues O += P V (M=128, N=64, K=128)
+//     with P read from its own tensor-memory columns;
 //   * two softmax warpgroups, one per subtile, one thread per query row:
 //     tcgen05.ld the row's 128 scores, mask, row maximum, exp2, row sum,
-//     round P to binary16 and tcgen05.st it back; rescale O in tensor memory
-//     when the maximum rose; at the end normalise and store O and the LSE.
-//   Subtile 0's softmax overlaps subtile 1's MMAs and vice versa.
+//     round P to binary16 and tcgen05.st it; rescale O in tensor memory when
+//     the row's reference maximum moves; at the end normalise and store O and
+//     the LSE.
+//   The subtiles are not kept in step: each one's softmax overlaps the other's
+//   MMAs and exp2 phase.
+//
+//   The reference maximum m a row's weights are taken against moves only when
+//   a tile's maximum exceeds it by more than kMaxSlack (8 in base-2 units), so
+//   the weights 2^(t - m) stay below 2^8 (well inside binary16) and O is
+//   rescaled only on such a jump instead of on every rise.  The folded sums
+//   are those of the page's recurrence with another choice of m; O / l and
+//   m + log2 l do not depend on that choice.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records
 // ATTN_ETIMEOUT in a device status word, drains what it has in flight, frees
@@ -91,6 +101,7 @@ constexpr uint32_t kSmemUsed = kOffAbort + 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
+constexpr float kMaxSlack = 8.f;  // a row's reference maximum moves only on a larger jump
 
 // Device scratch the kernel uses beyond its inputs and outputs: a status
 // word, and a ring of work-counter slots (next unit, finished CTAs), one slot
@@ -308,41 +319,72 @@ drain:
 // Each accumulation chain is issued by a single warp, so it stays ordered.
 
 // S issuer: S_s(j) as soon as the softmax has pulled S_s(j-1) into registers.
+// The two subtiles are served in whichever order their S buffers free up, so
+// neither subtile's pace is tied to the other's.
 __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
   uint32_t pos = 0;
-  uint32_t s_issued[2] = {0, 0};  // S MMAs issued per subtile (S-free is an "empty" barrier)
+  uint32_t s_issued0 = 0, s_issued1 = 0;  // S MMAs issued per subtile (S-free is an "empty" barrier)
   for (int k = 0;; ++k) {
     const int u = sy.next_unit(k);
     if (u == -1) return;
     if (u < 0) goto drain;
-    const Unit w = decode_unit(u, p);
-    const int qb = k & 1;
-    if (!sy.wait_warp(kBarQFull + qb, (k >> 1) & 1, 11)) goto drain;
-    tc_fence_after();
-    for (int j = 0; j < w.n1; ++j) {
-      const uint32_t kpos = pos + 2 * j;
-      const uint32_t kslot = kpos % kStages;
-      if (!sy.wait_warp(kBarKvFull + kslot, (kpos / kStages) & 1, 12)) goto drain;
+    {
+      const Unit w = decode_unit(u, p);
+      const int qb = k & 1;
+      if (!sy.wait_warp(kBarQFull + qb, (k >> 1) & 1, 11)) goto drain;
       tc_fence_after();
-      const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
+      const int n0 = w.n0, n1 = w.n1;
+      int j0 = 0, j1 = 0;
+      uint64_t t0 = 0;
+      uint32_t spins = 0;
+      while (j0 < n0 || j1 < n1) {
+        // the subtile that is behind first, then the other
+        const int first = (j0 <= j1) ? 0 : 1;
+        int pick = -1;
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        if (j >= (s ? w.n1 : w.n0)) continue;
-        if (!sy.wait_warp(kBarSFree + s, (s_issued[s] & 1) ^ 1, 13)) goto drain;
-        ++s_issued[s];
+        for (int c = 0; c < 2; ++c) {
+          const int s = first ^ c;
+          const int js = s ? j1 : j0;
+          if (js >= (s ? n1 : n0)) continue;
+          const uint32_t kpos = pos + 2 * js;
+          const uint32_t sfree_parity = ((s ? s_issued1 : s_issued0) & 1) ^ 1;
+          const bool ready = mbar_test_wait(sy.bar(kBarSFree + s), sfree_parity) &&
+                             mbar_test_wait(sy.bar(kBarKvFull + kpos % kStages), (kpos / kStages) & 1);
+          if (__all_sync(0xffffffffu, ready)) { pick = s; break; }
+        }
+        if (pick < 0) {
+          if (spins == 0) t0 = globaltimer_ns();
+          if ((++spins & 63u) == 0) {
+            if (*sy.abort_flag) goto drain;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *sy.abort_flag = 1;
+              atomicCAS(sy.status, 0, 13);
+              goto drain;
+            }
+          }
+          continue;
+        }
+        spins = 0;
         tc_fence_after();
+        const int s = pick;
+        const int j = s ? j1 : j0;
+        const uint32_t kslot = (pos + 2 * j) % kStages;
+        const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
         const uint32_t qbase = smem + kOffQ + (qb * 2 + s) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           mma_ss(tmem + kColS + 128u * s, sw128_desc(qbase + kk * 32), sw128_desc(kbase + kk * 32),
                  idS, kk > 0 ? 1u : 0u);
         mma_commit(sy.bar(kBarSFull + s));
+        if (s) { ++s_issued1; j1 = j + 1; } else { ++s_issued0; j0 = j + 1; }
+        // K(j) is released once every subtile that reads it has its S issued
+        const bool other_done = s ? (j0 > j || j >= n0) : (j1 > j || j >= n1);
+        if (other_done) mma_commit(sy.bar(kBarKvEmpty + kslot));
       }
-      mma_commit(sy.bar(kBarKvEmpty + kslot));  // K(j) read by both subtiles' S
+      mma_commit(sy.bar(kBarQEmpty + qb));  // every S of this unit issued
+      pos += 2 * w.n1;
     }
-    mma_commit(sy.bar(kBarQEmpty + qb));  // every S of this unit issued
-    pos += 2 * w.n1;
   }
 drain:
   mma_commit(sy.bar(kBarDrain + 0));
@@ -362,24 +404,25 @@ __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, u
     if (u < 0) goto drain;
     const Unit w = decode_unit(u, p);
     const int n = s ? w.n1 : w.n0;
-    for (int j = 0; j < w.n1; ++j) {
+    for (int j = 0; j < n; ++j) {
       const uint32_t vpos = pos + 2 * j + 1;
       const uint32_t vslot = vpos % kStages;
-      if (j < n) {
-        if (!sy.wait_warp(kBarPFull + s, pphase, 14)) goto drain;
-        pphase ^= 1;
-        if (!sy.wait_warp(kBarKvFull + vslot, (vpos / kStages) & 1, 10)) goto drain;
-        tc_fence_after();
-        const uint32_t vbase = smem + kOffRing + vslot * kTileBytes;
-        const uint32_t pcol = tmem + kColP + 64u * s;
+      if (!sy.wait_warp(kBarPFull + s, pphase, 14)) goto drain;
+      pphase ^= 1;
+      if (!sy.wait_warp(kBarKvFull + vslot, (vpos / kStages) & 1, 10)) goto drain;
+      tc_fence_after();
+      const uint32_t vbase = smem + kOffRing + vslot * kTileBytes;
+      const uint32_t pcol = tmem + kColP + 64u * s;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t bdesc = sw128_desc(vbase + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
-          mma_ts(tmem + kColO + 64u * s, pcol + 8u * kk, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(sy.bar(kBarPvDone + s));
+      for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        const uint64_t bdesc = sw128_desc(vbase + (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32);
+        mma_ts(tmem + kColO + 64u * s, pcol + 8u * kk, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
+      mma_commit(sy.bar(kBarPvDone + s));
       mma_commit(sy.bar(kBarKvEmpty + vslot));
+      // a V^T tile subtile 0 does not read: subtile 1 releases it for both, after
+      // its own wait on the tile, so the arrival cannot land in the slot's previous phase
+      if (j >= w.n0) mma_commit(sy.bar(kBarKvEmpty + vslot));
     }
     pos += 2 * w.n1;
   }
@@ -434,8 +477,11 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
         for (int a = 0; a < 8; ++a) mx8[a] = max3(mx8[a], sv[col + a], sv[col + 8 + a]);
       const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
                             fmaxf(mx8[6], mx8[7]));
-      const float m_new = fmaxf(m_run, mx * c);
-      const float alpha = ex2(m_run - m_new);
+      // the reference maximum moves only when this tile exceeds it by more than
+      // kMaxSlack (always on the first tile, where m_run = -inf)
+      const float mt = mx * c;
+      const float m_new = (mt > m_run + kMaxSlack) ? mt : m_run;
+      const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
       const float neg = -m_new;
       // P = 2^(S c - m'), in three dense passes so the SFU sees 128 back-to-back
       // exp2: paired fmas, then exp2, then paired row sums and binary16 packing
@@ -457,7 +503,7 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
         if (!sy.wait_warp(kBarPvDone + s, pvphase, 24 + s)) return;
         pvphase ^= 1;
         tc_fence_after();
-        // the maximum rose for some row of this warp: O *= 2^(m - m') (alpha = 1 elsewhere)
+        // the reference maximum moved for some row of this warp: O *= 2^(m - m') (alpha = 1 elsewhere)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t orow[64];
           tmem_ld_x64(tO, orow);
