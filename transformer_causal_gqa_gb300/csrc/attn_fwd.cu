@@ -339,8 +339,8 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
       uint64_t t0 = 0;
       uint32_t spins = 0;
       while (j0 < n0 || j1 < n1) {
-        // the subtile that is behind first, then the other
-        const int first = (j0 <= j1) ? 0 : 1;
+        // subtile 1 first, then subtile 0 (subtile 1 settles a little ahead)
+        const int first = 1;
         int pick = -1;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -603,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
 
   if (warp < 8) {
-    softmax_role(warp >> 2, p, sy, tmem);
+    // warps 0-3 take subtile 1 (the one a unit's last tile belongs to), warps 4-7 subtile 0
+    softmax_role(1 - (warp >> 2), p, sy, tmem);
   } else if (warp == kSWarp) {
     s_role(p, sy, smem, tmem);
   } else if (warp == kPvWarp0 || warp == kPvWarp0 + 1) {
