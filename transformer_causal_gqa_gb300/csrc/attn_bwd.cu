@@ -72,6 +72,14 @@ struct Sync {
     const bool ok = wait(i, parity, where);
     return __all_sync(0xffffffffu, ok);
   }
+  // Two waits taken together: both barriers are tested back to back, so a pair
+  // that is already complete costs one round trip instead of two.
+  __device__ bool wait2_warp(int i, uint32_t pi, int wi, int j, uint32_t pj, int wj) const {
+    const bool a = mbar_test_wait(bar(i), pi);
+    const bool b = mbar_test_wait(bar(j), pj);
+    if (__all_sync(0xffffffffu, a && b)) return true;
+    return wait_warp(i, pi, wi) && wait_warp(j, pj, wj);
+  }
   __device__ void drain_wait(int i, uint32_t parity) const {
     const uint32_t b = bar(i);
     const uint64_t t0 = globaltimer_ns();
@@ -214,8 +222,7 @@ __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint
     tc_fence_after();
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 112)) goto drain;
-      if (!sy.wait_warp(kBarSdFree, (pos & 1) ^ 1, 113)) goto drain;
+      if (!sy.wait2_warp(kBarKvFull + st, (pos / kStages) & 1, 112, kBarSdFree, (pos & 1) ^ 1, 113)) goto drain;
       tc_fence_after();
       const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
@@ -247,8 +254,7 @@ __device__ void dq_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint3
     const Unit w = decode(u, p);
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t st = pos % kStages, b = pos & 1;
-      if (!sy.wait_warp(kBarDsFull + b, (pos >> 1) & 1, 121)) goto drain;
-      if (!sy.wait_warp(kBarKvFull + st, (pos / kStages) & 1, 122)) goto drain;
+      if (!sy.wait2_warp(kBarDsFull + b, (pos >> 1) & 1, 121, kBarKvFull + st, (pos / kStages) & 1, 122)) goto drain;
       tc_fence_after();
       const uint32_t kb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
@@ -521,8 +527,7 @@ __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint
     tc_fence_after();
     for (int i = 0; i < w.steps; ++i, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 212)) goto drain;
-      if (!sy.wait_warp(kBarSFree, (pos & 1) ^ 1, 213)) goto drain;
+      if (!sy.wait2_warp(kBarQFull + st, (pos / kStages) & 1, 212, kBarSFree, (pos & 1) ^ 1, 213)) goto drain;
       tc_fence_after();
       const uint32_t sb = smem + kOffRing + st * kStageBytes;
 #pragma unroll
@@ -560,8 +565,7 @@ __device__ void acc_role(int which, const BwdParams &p, const Sync &sy, uint32_t
     const Unit w = decode(u, p);
     for (int i = 0; i < w.steps; ++i, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait_warp(kBarPFull, pos & 1, 221 + which)) goto drain;
-      if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 223 + which)) goto drain;
+      if (!sy.wait2_warp(kBarPFull, pos & 1, 221 + which, kBarQFull + st, (pos / kStages) & 1, 223 + which)) goto drain;
       tc_fence_after();
       const uint32_t bb = smem + kOffRing + st * kStageBytes + b_off;
 #pragma unroll
@@ -628,8 +632,7 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       const uint32_t st = pos % kStages;
       // the stage's copies (L and D among them) are visible to this thread once it
       // has seen the stage's barrier complete
-      if (!sy.wait_warp(kBarQFull + st, (pos / kStages) & 1, 230)) return;
-      if (!sy.wait_warp(kBarSFull, pos & 1, 231)) return;
+      if (!sy.wait2_warp(kBarQFull + st, (pos / kStages) & 1, 230, kBarSFull, pos & 1, 231)) return;
       tc_fence_after();
       uint32_t sr[64], dr[64];
       tmem_ld_2x64(tmem + lane_base + kColS + col0, tmem + lane_base + kColDP + col0, sr, dr);
@@ -652,8 +655,7 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       else
         key_step<false>(sr, dr, Ls, Ds, c, lo, hi, pp, pd);
       if (i > 0) {   // the previous step's products must be done before P^T, dS^T are overwritten
-        if (!sy.wait_warp(kBarDvDone, (pos - 1) & 1, 233)) return;
-        if (!sy.wait_warp(kBarDkDone, (pos - 1) & 1, 234)) return;
+        if (!sy.wait2_warp(kBarDvDone, (pos - 1) & 1, 233, kBarDkDone, (pos - 1) & 1, 234)) return;
         tc_fence_after();
       }
       tmem_st_2x32(tmem + lane_base + kColP + 32u * half, tmem + lane_base + kColDS + 32u * half, pp, pd);
@@ -662,8 +664,7 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       if (leader) mbar_arrive(sy.bar(kBarPFull));
     }
     // epilogue: the first half writes dV^T, the second s dK, for this key row
-    if (!sy.wait_warp(kBarDvDone, (pos - 1) & 1, 235)) return;
-    if (!sy.wait_warp(kBarDkDone, (pos - 1) & 1, 236)) return;
+    if (!sy.wait2_warp(kBarDvDone, (pos - 1) & 1, 235, kBarDkDone, (pos - 1) & 1, 236)) return;
     tc_fence_after();
     uint32_t ar[64];
     tmem_ld_x64(tmem + lane_base + (half ? kColDK : kColDV), ar);
