@@ -99,6 +99,32 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Paired IEEE binary32 arithmetic, one f32x2 instruction each:
+// (d0, d1) = (a0 b + c0, a1 b + c1)
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+// (d0, d1) = (p0 (q0 - r0), p1 (q1 - r1))
+__device__ __forceinline__ void mulsub2(float &d0, float &d1, float p0, float p1, float q0, float q1,
+                                        float r0, float r1) {
+  asm("{\n\t.reg .b64 rp, rq, rr, rd;\n\t"
+      "mov.b64 rp, {%2, %3};\n\t"
+      "mov.b64 rq, {%4, %5};\n\t"
+      "mov.b64 rr, {%6, %7};\n\t"
+      "sub.f32x2 rd, rq, rr;\n\t"
+      "mul.f32x2 rd, rp, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(p0), "f"(p1), "f"(q0), "f"(q1), "f"(r0), "f"(r1));
+}
+
 // 1-D bulk copy global -> shared, counted in bytes on `bar` (size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
@@ -327,18 +353,22 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
         const int lim = r - col0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, negL));
-          float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, negL));
+          float x0, x1, g0, g1;
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), c, negL, negL);
+          float p0 = ex2(x0), p1 = ex2(x1);
           if (2 * i > lim) p0 = 0.f;
           if (2 * i + 1 > lim) p1 = 0.f;
-          pk[i] = pack_half2(p0 * (__uint_as_float(dr[2 * i]) - D), p1 * (__uint_as_float(dr[2 * i + 1]) - D));
+          mulsub2(g0, g1, p0, p1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), D, D);
+          pk[i] = pack_half2(g0, g1);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, negL));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, negL));
-          pk[i] = pack_half2(p0 * (__uint_as_float(dr[2 * i]) - D), p1 * (__uint_as_float(dr[2 * i + 1]) - D));
+          float x0, x1, g0, g1;
+          fma2(x0, x1, __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]), c, negL, negL);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          mulsub2(g0, g1, p0, p1, __uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]), D, D);
+          pk[i] = pack_half2(g0, g1);
         }
       }
       if (pos >= 2) {   // the product that read this dS buffer two steps ago must be complete
@@ -596,13 +626,18 @@ __device__ __forceinline__ void key_step(const uint32_t (&sr)[64], const uint32_
     const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
     float pv[4], dv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4; e += 2) {
       const int t = 4 * t4 + e;
-      const float pr = ex2(fmaf(__uint_as_float(sr[t]), c, -Lv[e]));
-      const float g = pr * (__uint_as_float(dr[t]) - Dv[e]);
-      const bool live = !kMasked || (t >= lo && t < hi);
-      pv[e] = live ? pr : 0.f;
-      dv[e] = live ? g : 0.f;
+      float x0, x1, g0, g1;
+      fma2(x0, x1, __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c, -Lv[e], -Lv[e + 1]);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      mulsub2(g0, g1, p0, p1, __uint_as_float(dr[t]), __uint_as_float(dr[t + 1]), Dv[e], Dv[e + 1]);
+      const bool live0 = !kMasked || (t >= lo && t < hi);
+      const bool live1 = !kMasked || (t + 1 >= lo && t + 1 < hi);
+      pv[e] = live0 ? p0 : 0.f;
+      dv[e] = live0 ? g0 : 0.f;
+      pv[e + 1] = live1 ? p1 : 0.f;
+      dv[e + 1] = live1 ? g1 : 0.f;
     }
     pp[2 * t4] = pack_half2(pv[0], pv[1]);
     pp[2 * t4 + 1] = pack_half2(pv[2], pv[3]);
