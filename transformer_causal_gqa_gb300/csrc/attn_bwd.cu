@@ -615,28 +615,36 @@ drain:
 // One key row's step over the thread's 64 query columns: P^T = 2^(S^T c - L)
 // and dS^T = P^T (dP^T - D), packed to binary16 pairs (query columns 2m,
 // 2m+1 in [m]).  With kMasked, column t is kept only when lo <= t < hi.
+// Three passes (the exponents, then the 64 exp2 back to back, then dS^T and
+// the packing) keep the SFU fed while the other pipes work on the neighbours.
 template <bool kMasked>
 __device__ __forceinline__ void key_step(const uint32_t (&sr)[64], const uint32_t (&dr)[64],
                                          const float *Ls, const float *Ds, float c, int lo, int hi,
                                          uint32_t (&pp)[32], uint32_t (&pd)[32]) {
+  float pf[64];
 #pragma unroll
   for (int t4 = 0; t4 < 16; ++t4) {
     const float4 L4 = *reinterpret_cast<const float4 *>(Ls + 4 * t4);
+    fma2(pf[4 * t4], pf[4 * t4 + 1], __uint_as_float(sr[4 * t4]), __uint_as_float(sr[4 * t4 + 1]), c, -L4.x, -L4.y);
+    fma2(pf[4 * t4 + 2], pf[4 * t4 + 3], __uint_as_float(sr[4 * t4 + 2]), __uint_as_float(sr[4 * t4 + 3]), c, -L4.z, -L4.w);
+  }
+#pragma unroll
+  for (int t = 0; t < 64; ++t) pf[t] = ex2(pf[t]);
+#pragma unroll
+  for (int t4 = 0; t4 < 16; ++t4) {
     const float4 D4 = *reinterpret_cast<const float4 *>(Ds + 4 * t4);
-    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w}, Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+    const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
     float pv[4], dv[4];
 #pragma unroll
     for (int e = 0; e < 4; e += 2) {
       const int t = 4 * t4 + e;
-      float x0, x1, g0, g1;
-      fma2(x0, x1, __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c, -Lv[e], -Lv[e + 1]);
-      const float p0 = ex2(x0), p1 = ex2(x1);
-      mulsub2(g0, g1, p0, p1, __uint_as_float(dr[t]), __uint_as_float(dr[t + 1]), Dv[e], Dv[e + 1]);
+      float g0, g1;
+      mulsub2(g0, g1, pf[t], pf[t + 1], __uint_as_float(dr[t]), __uint_as_float(dr[t + 1]), Dv[e], Dv[e + 1]);
       const bool live0 = !kMasked || (t >= lo && t < hi);
       const bool live1 = !kMasked || (t + 1 >= lo && t + 1 < hi);
-      pv[e] = live0 ? p0 : 0.f;
+      pv[e] = live0 ? pf[t] : 0.f;
       dv[e] = live0 ? g0 : 0.f;
-      pv[e + 1] = live1 ? p1 : 0.f;
+      pv[e + 1] = live1 ? pf[t + 1] : 0.f;
       dv[e + 1] = live1 ? g1 : 0.f;
     }
     pp[2 * t4] = pack_half2(pv[0], pv[1]);
