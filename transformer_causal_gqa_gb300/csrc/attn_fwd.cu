@@ -449,8 +449,13 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
     const int n = s ? w.n1 : w.n0;
     const int diag = 2 * w.b + s;
     float m_run = -INFINITY, l_run = 0.f;
+    // S_s(j+1) is tested (without blocking) right after P_s(j) is handed over; when
+    // it was already complete the next tile skips its wait.  Each barrier test
+    // costs a shared-memory round trip in the running kernel, and this one overlaps
+    // the loop's turn instead of sitting in front of the next tile.
+    bool s_seen = false;
     for (int j = 0; j < n; ++j) {
-      if (!sy.wait_warp(kBarSFull + s, sphase, 20 + s)) return;
+      if (!__all_sync(0xffffffffu, s_seen) && !sy.wait_warp(kBarSFull + s, sphase, 20 + s)) return;
       sphase ^= 1;
       tc_fence_after();
       uint32_t sr[128];
@@ -523,6 +528,7 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarPFull + s));
       m_run = m_new;
+      s_seen = j + 1 < n && mbar_test_wait(sy.bar(kBarSFull + s), sphase);
     }
     // epilogue: O / l and m + log2 l once the last P V is done
     if (!sy.wait_warp(kBarPvDone + s, pvphase, 22 + s)) return;
