@@ -150,3 +150,41 @@ def test_rejections_on_device():
         tcg.attn_fwd(q, k, vT, q.view(128, 256), lse, 128, 4, 2, 0.18)
     assert e.value.status == tcg.ATTN_EOVERLAP
     assert tcg.last_device_status() == tcg.ATTN_OK
+
+
+def compare_arrays(q, k, vT, T, H, G):
+    c = synthetic.scale_c()
+    o, lse = run_gpu(q, k, vT, T, H, G, c)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, vT, T, H, G, c)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    d_o = float(np.abs(o - o_ref).max())
+    d_l = float(np.abs(lse - lse_ref).max())
+    assert d_o <= TOL_O, f"max |dO| = {d_o}"
+    assert d_l <= TOL_LSE, f"max |dLSE| = {d_l}"
+
+
+@pytest.mark.parametrize("jump", [6.0, 12.0, 40.0, 120.0])
+def test_late_score_jump(jump):
+    """A key late in the sequence whose score exceeds every earlier one by `jump`
+    (base-2 units) for every query row after it.  Below 8 the rows keep their
+    reference maximum (weights up to 2^jump); above it they move the reference and
+    rescale O and l by 2^-jump or less (to zero in binary32 for the largest
+    jumps).  Both paths must match the exact definition."""
+    T, H, G = 1024, 2, 1
+    w = synthetic.custom(T, H, G, seed=1234)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    j = 700                                        # key tile 5, row 60 of that tile
+    u = np.zeros(64, dtype=np.float64)
+    u[0] = 1.0
+    q = q.astype(np.float64)
+    q[:, :, 0] = 4.0                               # every query row: component 4 along u
+    # score of key j for every row: 4 * k0 * scale/ln2 = jump + (largest earlier score)
+    base_max = float(np.max(q[:, :, :] @ k[0].astype(np.float64).T * c))
+    k = k.astype(np.float64)
+    k[0, j, :] = 0.0
+    k[0, j, 0] = (jump + base_max) / (4.0 * c)
+    q16 = q.astype(np.float16)
+    k16 = k.astype(np.float16)
+    assert np.isfinite(k16).all()
+    compare_arrays(q16, k16, vT, T, H, G)
