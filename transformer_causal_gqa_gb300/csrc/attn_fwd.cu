@@ -319,8 +319,11 @@ drain:
 // Each accumulation chain is issued by a single warp, so it stays ordered.
 
 // S issuer: S_s(j) as soon as the softmax has pulled S_s(j-1) into registers.
-// The two subtiles are served in whichever order their S buffers free up, so
-// neither subtile's pace is tied to the other's.
+// The two subtiles are served in whichever order their S buffers free up
+// (subtile 1 is tested first), not strictly in turn.  Issued strictly in turn,
+// both subtiles' S became ready together and their softmax warpgroups ran in
+// lockstep, meeting on the SFU; served this way, one pick every ~1000 cycles
+// keeps them about half a tile apart.
 __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
   uint32_t pos = 0;
