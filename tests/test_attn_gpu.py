@@ -163,13 +163,17 @@ def compare_arrays(q, k, vT, T, H, G):
     assert d_l <= TOL_LSE, f"max |dLSE| = {d_l}"
 
 
-@pytest.mark.parametrize("jump", [6.0, 12.0, 40.0, 120.0])
+@pytest.mark.parametrize("jump", [6.0, 12.0, 14.0, 16.0, 40.0, 120.0, 200.0])
 def test_late_score_jump(jump):
     """A key late in the sequence whose score exceeds every earlier one by `jump`
-    (base-2 units) for every query row after it.  Below 8 the rows keep their
-    reference maximum (weights up to 2^jump); above it they move the reference and
-    rescale O and l by 2^-jump or less (to zero in binary32 for the largest
-    jumps).  Both paths must match the exact definition."""
+    (base-2 units) for every query row after it.  Each row's weight for that key
+    is 2^(jump + d) against its reference maximum, d >= 0 the row's own gap to
+    the largest earlier score.  Below the slack of 8 a row keeps its reference
+    (weights up to 2^8); above it the reference moves to the tile's maximum and O
+    and l are scaled by 2^-jump or less (to zero in binary32 for the largest
+    jumps).  Jumps of 14 and 16 put the rows of one warp on both sides of the
+    line where a weight against the old reference would pass the largest
+    binary16.  Every case must match the exact definition."""
     T, H, G = 1024, 2, 1
     w = synthetic.custom(T, H, G, seed=1234)
     q, k, vT = synthetic.make_inputs(w)
@@ -184,6 +188,30 @@ def test_late_score_jump(jump):
     k = k.astype(np.float64)
     k[0, j, :] = 0.0
     k[0, j, 0] = (jump + base_max) / (4.0 * c)
+    q16 = q.astype(np.float16)
+    k16 = k.astype(np.float16)
+    assert np.isfinite(k16).all()
+    compare_arrays(q16, k16, vT, T, H, G)
+
+
+@pytest.mark.parametrize("rise", [1.0, 3.0, 9.0])
+def test_tile_wide_rise(rise):
+    """Every key of one tile scores `rise` above the largest earlier score, for
+    every query row after the tile: 128 equal weights of at least 2^rise, tied at
+    the tile's maximum.  With rises 1 and 3 most rows keep their reference (row
+    sums of 256 to over 1000 against it), with rise 9 every row moves it.  The
+    diagonal tile's mask (query rows inside the tile) is covered too."""
+    T, H, G = 1024, 4, 2
+    w = synthetic.custom(T, H, G, seed=4321)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    q = q.astype(np.float64)
+    q[:, :, 0] = 4.0
+    base_max = float(max(np.max(q[h] @ k[h // (H // G)].astype(np.float64).T * c) for h in range(H)))
+    k = k.astype(np.float64)
+    for g in range(G):
+        k[g, 640:768, :] = 0.0                      # key tile 5
+        k[g, 640:768, 0] = (rise + base_max) / (4.0 * c)
     q16 = q.astype(np.float16)
     k16 = k.astype(np.float16)
     assert np.isfinite(k16).all()
