@@ -79,7 +79,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default=synthetic.HEADLINE, choices=list(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default=synthetic.HEADLINE,
+                    choices=list(synthetic.WORKLOADS) + list(synthetic.PROFILE_SHAPES))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=120.0,
@@ -275,7 +276,7 @@ def run_gb300(args):
         dist.barrier()
     tcg.load_library()
 
-    base = synthetic.WORKLOADS[args.workload]
+    base = synthetic.lookup(args.workload)
     w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     c = synthetic.scale_c()
@@ -388,7 +389,7 @@ def run_reference(args, metric=METRIC):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    w = synthetic.WORKLOADS[args.workload]
+    w = synthetic.lookup(args.workload)
     inputs = synthetic.make_inputs(w)
     K, W = max(1, args.steps), max(3, args.warmup)
     budget_s = args.reference_budget_s
@@ -477,7 +478,7 @@ def run_gb300_backward(args):
         dist.barrier()
     tcg.load_library()
 
-    base = synthetic.WORKLOADS[args.workload]
+    base = synthetic.lookup(args.workload)
     w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     dO_np = synthetic.make_output_grad(w)
@@ -610,7 +611,7 @@ def run_reference_backward(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    w = synthetic.WORKLOADS[args.workload]
+    w = synthetic.lookup(args.workload)
     inputs = synthetic.make_inputs(w)
     dO = synthetic.make_output_grad(w)
     o, lse = bwd_oracle_inputs(w, inputs)
@@ -684,7 +685,7 @@ def run_gb300_materialised(args):
     if world > 1:
         dist.barrier()
     tcg.load_library()
-    base = synthetic.WORKLOADS[args.workload]
+    base = synthetic.lookup(args.workload)
     w = rank_problem(base, rank)
     inputs = synthetic.make_inputs(w)
     c = synthetic.scale_c()
@@ -837,7 +838,7 @@ def run_gb300_producer(args):
     if world > 1:
         dist.barrier()
     tcg.load_library()
-    base = synthetic.WORKLOADS[args.workload]
+    base = synthetic.lookup(args.workload)
     w = rank_problem(base, rank)
     T, H, G = w.T, w.heads, w.kv_heads
     width, n_out, flops = producer_shape(w)
@@ -957,7 +958,7 @@ def run_reference_producer(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    w = synthetic.WORKLOADS[args.workload]
+    w = synthetic.lookup(args.workload)
     width, n_out, _ = producer_shape(w)
     host = synthetic.make_producer_inputs(w.T, width, w.heads, w.kv_heads, w.seed)
     K, W = max(1, args.steps), max(3, args.warmup)

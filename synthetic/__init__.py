@@ -78,6 +78,23 @@ WORKLOADS = {
 }
 HEADLINE = "t8192_h32_kv8"
 
+# Shapes for profiler captures only, not benchmark workloads: the headline length with
+# fewer heads, so that a capture holds a few GB of device memory while the rows of the
+# materialised planes are as long as the headline's.
+PROFILE_SHAPES = {
+    w.name: w
+    for w in [
+        Workload("t8192_h4_kv1_profile", 8192, 4, 1, seed=0x5EED0005),
+    ]
+}
+
+
+def lookup(name: str) -> Workload:
+    """A benchmark workload or a profiling shape, by name."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    return PROFILE_SHAPES[name]
+
 
 def custom(T: int, heads: int, kv_heads: int, seed: int, **kw) -> Workload:
     return Workload(f"t{T}_h{heads}_kv{kv_heads}_s{seed}", T, heads, kv_heads, seed, **kw)

@@ -32,6 +32,14 @@ def test_workload_table():
         assert w.T % 64 == 0 and w.heads % w.kv_heads == 0
 
 
+def test_profile_shapes_apart_from_workloads():
+    assert not set(synthetic.PROFILE_SHAPES) & set(synthetic.WORKLOADS)
+    for name, w in synthetic.PROFILE_SHAPES.items():
+        assert synthetic.lookup(name) is w
+        assert w.T % 64 == 0 and w.heads % w.kv_heads == 0
+    assert synthetic.lookup(synthetic.HEADLINE) is synthetic.WORKLOADS[synthetic.HEADLINE]
+
+
 def test_peaked_and_outlier_recipes():
     w = synthetic.custom(388, 2, 1, seed=5, qk_scale=4.0)
     q, k, _ = synthetic.make_inputs(w)

@@ -69,12 +69,15 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ---------------------------------------------------------------------------- scores
 // Block (kt, qt) of head h: grid.x enumerates the causal tiles (qt, kt <= qt).
-// Shared memory: the Q and K tiles, then the binary32 result staged as four
-// 32-column boxes of 128 rows (128-byte swizzle) for the TMA store.
-constexpr uint32_t kStageOff = 2 * kTileBytes;
+// Shared memory: the Q and K tiles, then -- over them, once the MMAs that read
+// them are complete -- the binary32 result staged as four 32-column boxes of
+// 128 rows (128-byte swizzle) for the TMA store.  64 KiB per CTA lets three
+// CTAs share an SM (3 x 128 tensor-memory columns), so one CTA's store overlaps
+// another's loads and products.
+constexpr uint32_t kStageOff = 0;
 constexpr uint32_t kBoxBytes = kTile * 32 * 4;       // 16 KiB
 constexpr uint32_t kScoresBarOff = kStageOff + 4 * kBoxBytes;
-constexpr uint32_t kScoresSmem = kScoresBarOff + 64 + 1024;   // two CTAs per SM: 2 x 128 TMEM columns
+constexpr uint32_t kScoresSmem = kScoresBarOff + 64 + 1024;
 
 __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                      const __grid_constant__ CUtensorMap tmK,
@@ -158,6 +161,7 @@ __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUt
       tma_store_commit_wait();
     } else {
       // let a copy that is still in flight land before the shared memory is released
+      // (the values staged over it are discarded)
       wait_bounded(bar_full, 0, p.status, 303);
     }
   }
@@ -171,16 +175,35 @@ __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUt
 // One warp per (row i, head h), eight rows per CTA.  Pass 1 streams the row's
 // causal scores once (a float4 per lane per step), keeping per lane a running
 // maximum m of t = S c and a sum l = sum 2^(t - m) rescaled whenever m rises;
-// the lanes' pairs are then merged.  Pass 2 reads the scores again (the row
-// was just read, so mostly from L2) and writes the normalised binary16
-// probabilities, zero-filled to the end of the diagonal tile.  (Holding the
-// row in registers instead, over four warps, measured slower: it halves the
-// rows in flight per SM.)
+// the lanes' pairs are then merged.  Pass 2 reads the scores again and writes
+// the normalised binary16 probabilities, zero-filled to the end of the
+// diagonal tile.  The rows in flight (up to 32 KiB each) outgrow L2 at large T,
+// so pass 2 walks the row backwards (its end, read last, is the likeliest to
+// be in L2) and marks its loads and the probability stores evict-first: a
+// score is not read a third time, and those lines give way to the rows still
+// waiting for their second read.  (Holding the row in registers instead, over
+// four warps, measured slower: it halves the rows in flight per SM.)
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
   return m_old == -INFINITY ? 0.f : ex2(m_old - m_new);
 }
 
+// 16-byte load and 8-byte store with an L2 eviction policy from createpolicy.
+__device__ __forceinline__ float4 ld_policy(const float *ptr, uint64_t pol) {
+  float4 v;
+  asm("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_policy(void *ptr, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "l"(pol)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(256) softmax_kernel(const MatParams p) {
+  uint64_t evict_first;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 8 + warp, h = blockIdx.y;
   if (i >= p.T) return;
@@ -212,11 +235,14 @@ __global__ void __launch_bounds__(256) softmax_kernel(const MatParams p) {
   }
   const float inv = 1.f / l;
   if (lane == 0) p.lse[(size_t)h * p.T + i] = m + log2f(l);
+  const int nsteps = (end + 127) / 128;
 #pragma unroll 4
-  for (int j0 = 4 * lane; j0 < end; j0 += 128) {
+  for (int st = nsteps - 1; st >= 0; --st) {
+    const int j0 = 128 * st + 4 * lane;
+    if (j0 >= end) continue;
     float q[4] = {0.f, 0.f, 0.f, 0.f};
     if (j0 < n) {
-      const float4 a = *reinterpret_cast<const float4 *>(srow + j0);
+      const float4 a = ld_policy(srow + j0, evict_first);
       const float t[4] = {a.x * c, a.y * c, a.z * c, a.w * c};
 #pragma unroll
       for (int e = 0; e < 4; ++e) q[e] = j0 + e < n ? ex2(t[e] - m) * inv : 0.f;
@@ -225,7 +251,7 @@ __global__ void __launch_bounds__(256) softmax_kernel(const MatParams p) {
     uint2 v;
     v.x = *reinterpret_cast<uint32_t *>(&lo);
     v.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(prow + j0) = v;
+    st_policy(prow + j0, v, evict_first);
   }
 }
 
