@@ -472,8 +472,9 @@ constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarKvFull = 0, kBarKvEmpty = 1;
 constexpr int kBarQFull = 2, kBarQEmpty = 2 + kStages;
 constexpr int kBarSFull = 2 + 2 * kStages, kBarSFree = kBarSFull + 1;   // S^T and dP^T together
-constexpr int kBarPFull = kBarSFree + 1, kBarDvDone = kBarPFull + 1, kBarDkDone = kBarDvDone + 1;
-constexpr int kBarDrain = kBarDkDone + 1;        // + issuer warp (0..2)
+// per query-column half h: P^T, dS^T written (PFull + h), dV and dK products of it done (Done + h)
+constexpr int kBarPFull = kBarSFree + 1, kBarDone = kBarPFull + 2;
+constexpr int kBarDrain = kBarDone + 2;          // + issuer warp (0..2)
 constexpr int kNumBars = kBarDrain + 3;
 constexpr uint32_t kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
@@ -580,7 +581,10 @@ drain:
 }
 
 // dV += P^T dO (B = dO tile) when which == 0, dK += dS^T Q (B = Q tile) when
-// which == 1; B is read MN-major from the tile.
+// which == 1; B is read MN-major from the tile.  The products run over the step's
+// two halves of query columns (K = 64 each), each as soon as the compute warps of
+// that half have written it, and each half's completion is signalled on its own
+// barrier: a half's next P^T, dS^T wait only for the products that read its own.
 __device__ void acc_role(int which, const BwdParams &p, const Sync &sy, uint32_t smem,
                          uint32_t tmem) {
   constexpr uint32_t id = idesc_f16_f32_mn(kTile, kD, false, true);
@@ -588,21 +592,28 @@ __device__ void acc_role(int which, const BwdParams &p, const Sync &sy, uint32_t
   const uint32_t a_col = which ? kColDS : kColP;
   const uint32_t d_col = which ? kColDK : kColDV;
   const uint32_t b_off = which ? kSQ : kSDO;
-  const int done_bar = which ? kBarDkDone : kBarDvDone;
   uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
     const Unit w = decode(u, p);
     for (int i = 0; i < w.steps; ++i, ++pos) {
       const uint32_t st = pos % kStages;
-      if (!sy.wait2_warp(kBarPFull, pos & 1, 221 + which, kBarQFull + st, (pos / kStages) & 1, 223 + which)) goto drain;
-      tc_fence_after();
       const uint32_t bb = smem + kOffRing + st * kStageBytes + b_off;
+      // each half of the query columns as soon as its P^T, dS^T are written
 #pragma unroll
-      for (int e = 0; e < kTile / 16; ++e)
-        mma_ts(tmem + d_col, tmem + a_col + 8u * e, sw128_mn_desc(bb + e * 2048, kHalfTileBytes),
-               id, (i > 0 || e > 0) ? 1u : 0u);
-      mma_commit(sy.bar(done_bar));
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 0) {
+          if (!sy.wait2_warp(kBarPFull, pos & 1, 221 + which, kBarQFull + st, (pos / kStages) & 1, 223 + which)) goto drain;
+        } else if (!sy.wait_warp(kBarPFull + 1, pos & 1, 225 + which)) {
+          goto drain;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int e = 4 * hh; e < 4 * hh + 4; ++e)
+          mma_ts(tmem + d_col, tmem + a_col + 8u * e, sw128_mn_desc(bb + e * 2048, kHalfTileBytes),
+                 id, (i > 0 || e > 0) ? 1u : 0u);
+        mma_commit(sy.bar(kBarDone + hh));
+      }
       mma_commit(sy.bar(kBarQEmpty + st));
     }
   }
@@ -697,17 +708,17 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
         key_step<true>(sr, dr, Ls, Ds, c, lo, hi, pp, pd);
       else
         key_step<false>(sr, dr, Ls, Ds, c, lo, hi, pp, pd);
-      if (i > 0) {   // the previous step's products must be done before P^T, dS^T are overwritten
-        if (!sy.wait2_warp(kBarDvDone, (pos - 1) & 1, 233, kBarDkDone, (pos - 1) & 1, 234)) return;
+      if (i > 0) {   // the previous step's products of this half must be done before its P^T, dS^T are overwritten
+        if (!sy.wait_warp(kBarDone + half, (pos - 1) & 1, 233)) return;
         tc_fence_after();
       }
       tmem_st_2x32(tmem + lane_base + kColP + 32u * half, tmem + lane_base + kColDS + 32u * half, pp, pd);
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(sy.bar(kBarPFull));
+      if (leader) mbar_arrive(sy.bar(kBarPFull + half));
     }
     // epilogue: the first half writes dV^T, the second s dK, for this key row
-    if (!sy.wait2_warp(kBarDvDone, (pos - 1) & 1, 235, kBarDkDone, (pos - 1) & 1, 236)) return;
+    if (!sy.wait2_warp(kBarDone, (pos - 1) & 1, 235, kBarDone + 1, (pos - 1) & 1, 236)) return;
     tc_fence_after();
     uint32_t ar[64];
     tmem_ld_x64(tmem + lane_base + (half ? kColDK : kColDV), ar);
@@ -750,9 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sy.bar(kBarSFull), 1);
     mbar_init(sy.bar(kBarSFree), kComputeWarps);
-    mbar_init(sy.bar(kBarPFull), kComputeWarps);
-    mbar_init(sy.bar(kBarDvDone), 1);
-    mbar_init(sy.bar(kBarDkDone), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(sy.bar(kBarPFull + h), kComputeWarps / 2);
+      mbar_init(sy.bar(kBarDone + h), 2);   // the dV and the dK issuer
+    }
     for (int i = 0; i < 3; ++i) mbar_init(sy.bar(kBarDrain + i), 1);
     *sy.abort_flag = 0;
     mbar_fence_init();
