@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dP^T at 128 (fp32), P^T at 256, dS^T at 320 (binary16 pairs), dV at 384,
 // dK at 448 (fp32).
 namespace klaunch {
-constexpr int kStages = 4;   // ring of {Q tile, dO tile, L, D}
+constexpr int kStages = 5;   // ring of {Q tile, dO tile, L, D}
 constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;   // L and D: 512 bytes each
 constexpr uint32_t kOffK = 0;                              // K tile, V^T tile
 constexpr uint32_t kOffRing = 2 * kTileBytes;
