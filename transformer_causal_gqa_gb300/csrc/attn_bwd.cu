@@ -460,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // query tiles kt .. q_tiles-1, accumulating dK and dV over all of them.
 // Eight compute warps: warp w serves lanes 32 (w % 4) .. +31 (one key per
 // thread) and query columns 64 (w / 4) .. +63; as in the query launch, S^T
-// and dP^T arrive and are released together.  Tensor memory: S^T at 0,
+// and dP^T arrive and are released together, while P^T and dS^T go to the
+// dV and dK products one column half at a time.  Tensor memory: S^T at 0,
 // dP^T at 128 (fp32), P^T at 256, dS^T at 320 (binary16 pairs), dV at 384,
 // dK at 448 (fp32).
 namespace klaunch {
