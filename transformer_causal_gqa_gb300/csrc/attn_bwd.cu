@@ -166,12 +166,13 @@ __device__ __forceinline__ int unit_of(int k, int units) {
 // both at once (so the next pair is formed while this one is processed), and
 // forms P and dS in one pass.  Tensor memory: S at 0, dP at 128 (fp32), dS in
 // two buffers at 256 and 320 (binary16 pairs, so a step need not wait for the
-// previous dQ product), dQ at 384 (fp32, 64 columns).
+// previous dQ product), dQ at 384 (fp32, 64 columns).  The unit's O tile comes
+// with its Q and dO tiles, so the row term D is formed from shared memory.
 namespace qlaunch {
 constexpr int kStages = 4;                       // ring of {K tile, V^T tile}
 constexpr uint32_t kStageBytes = 2 * kTileBytes;
-constexpr uint32_t kOffQ = 0;                    // Q tile, dO tile
-constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffQ = 0;                    // Q tile, dO tile, O tile
+constexpr uint32_t kOffRing = 3 * kTileBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr int kBarQFull = 0, kBarQEmpty = 1;
 constexpr int kBarKvFull = 2, kBarKvEmpty = 2 + kStages;
@@ -199,9 +200,9 @@ __device__ __forceinline__ Unit decode(int u, const BwdParams &p) {
   w.nk = w.qt + 1;
   return w;
 }
-__device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const CUtensorMap *tmK,
-                          const CUtensorMap *tmVT, const BwdParams &p, const Sync &sy,
-                          uint32_t smem) {
+__device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const CUtensorMap *tmO,
+                          const CUtensorMap *tmK, const CUtensorMap *tmVT, const BwdParams &p,
+                          const Sync &sy, uint32_t smem) {
   const int units = p.heads * p.q_tiles;
   uint32_t pos = 0, pos_issued = 0, q_issued = 0;
   int k = 0;
@@ -209,9 +210,10 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmDO, const
     const Unit w = decode(u, p);
     if (!sy.wait(kBarQEmpty, (k & 1) ^ 1, 101)) goto drain;
     ++q_issued;
-    mbar_arrive_expect_tx(sy.bar(kBarQFull), 2 * kTileBytes);
+    mbar_arrive_expect_tx(sy.bar(kBarQFull), 3 * kTileBytes);
     tma_load_3d(smem + kOffQ, tmQ, sy.bar(kBarQFull), 0, w.qt * kTile, w.h);
     tma_load_3d(smem + kOffQ + kTileBytes, tmDO, sy.bar(kBarQFull), w.h * kD, w.qt * kTile, 0);
+    tma_load_3d(smem + kOffQ + 2 * kTileBytes, tmO, sy.bar(kBarQFull), w.h * kD, w.qt * kTile, 0);
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t st = pos % kStages;
       if (!sy.wait(kBarKvEmpty + st, ((pos / kStages) & 1) ^ 1, 102)) goto drain;
@@ -297,7 +299,8 @@ drain:
   sy.drain_wait(kBarDrain + 1, 0);
 }
 
-__device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) {
+__device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *smem_gen,
+                             uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
   const int r = 32 * (warp & 3) + (threadIdx.x & 31);   // tile row (tensor-memory lane)
   const int half = warp >> 2;                            // key columns 64 half .. +63
@@ -312,16 +315,18 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
     const Unit w = decode(u, p);
     const int row = w.qt * kTile + r;
     const bool valid = row < p.T;
-    // the row term D = rowsum(dO O) and the forward's L for this row
+    // the row term D = rowsum(dO O), from the unit's dO and O tiles in shared memory
+    // (128-byte swizzled rows: chunk i of row r at i ^ (r mod 8)), and the forward's L
+    if (!sy.wait_warp(kBarQFull, k & 1, 135)) return;
     float L = 0.f, D = 0.f;
     if (valid) {
-      const size_t at = ((size_t)row * p.heads + w.h) * kD;
-      const uint4 *go = reinterpret_cast<const uint4 *>(p.dO + at);
-      const uint4 *oo = reinterpret_cast<const uint4 *>(p.o + at);
+      const uint8_t *rdo = smem_gen + kOffQ + kTileBytes + r * 128;
+      const uint8_t *ro = smem_gen + kOffQ + 2 * kTileBytes + r * 128;
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 a = go[i], b = oo[i];
+        const uint4 a = *reinterpret_cast<const uint4 *>(rdo + ((i ^ (r & 7)) << 4));
+        const uint4 b = *reinterpret_cast<const uint4 *>(ro + ((i ^ (r & 7)) << 4));
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -335,6 +340,9 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
       L = p.lse[(size_t)w.h * p.T + row];
       if (half == 0) p.D[(size_t)w.h * p.T + row] = D;
     }
+    // the Q buffer (with dO and O) may be refilled once the products and these reads are done
+    __syncwarp();
+    if (leader) mbar_arrive(sy.bar(kBarQEmpty));
     const float negL = -L;
     for (int j = 0; j < w.nk; ++j, ++pos) {
       const uint32_t b = pos & 1;
@@ -398,8 +406,8 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, uint32_t tmem) 
 
 __global__ void __launch_bounds__(kThreads, 1)
     query_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmVT,
-                 const BwdParams p) {
+                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmVT, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t smem = (raw + 1023u) & ~1023u;
@@ -411,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sy.status = p.status;
   if (warp == kWarpLoad && lane == 0) {
     mbar_init(sy.bar(kBarQFull), 1);
-    mbar_init(sy.bar(kBarQEmpty), 1);
+    mbar_init(sy.bar(kBarQEmpty), 1 + kComputeWarps);   // the S/dP issuer's commit, the row-term reads
     for (int i = 0; i < kStages; ++i) {
       mbar_init(sy.bar(kBarKvFull + i), 1);
       mbar_init(sy.bar(kBarKvEmpty + i), 2);   // S/dP issuer and dQ issuer
@@ -436,13 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
   if (warp < kComputeWarps) {
-    compute_role(p, sy, tmem);
+    compute_role(p, sy, smem_gen, tmem);
   } else if (warp == kWarpSdp) {
     sdp_role(p, sy, smem, tmem);
   } else if (warp == kWarpDq) {
     dq_role(p, sy, smem, tmem);
   } else if (warp == kWarpLoad) {
-    if (lane == 0) load_role(&tmQ, &tmDO, &tmK, &tmVT, p, sy, smem);
+    if (lane == 0) load_role(&tmQ, &tmDO, &tmO, &tmK, &tmVT, p, sy, smem);
     __syncwarp();
   }
   tc_fence_before();
@@ -915,11 +923,13 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   if ((rc = bwd_state(&st))) return rc;
 
   const uint64_t rowb = kD * 2, trow = (uint64_t)T * 2;
-  CUtensorMap tmQ, tmK, tmVT, tmDO;
+  CUtensorMap tmQ, tmK, tmVT, tmDO, tmO;
   if (!encode_3d(&tmQ, q, kD, T, heads, rowb, rowb * T, kD, kTile) ||
       !encode_3d(&tmK, k, kD, T, kv_heads, rowb, rowb * T, kD, kTile) ||
       !encode_3d(&tmVT, vT, T, kD, kv_heads, trow, trow * kD, kTile / 2, kD) ||
       !encode_3d(&tmDO, dO, (uint64_t)heads * kD, T, 1, (uint64_t)heads * kD * 2,
+                 (uint64_t)heads * kD * 2 * T, kD, kTile) ||
+      !encode_3d(&tmO, o, (uint64_t)heads * kD, T, 1, (uint64_t)heads * kD * 2,
                  (uint64_t)heads * kD * 2 * T, kD, kTile))
     return ATTN_ELAUNCH;
 
@@ -942,7 +952,7 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   p.stall = g_bwd_stall.exchange(0);
   const int qunits = heads * p.q_tiles, kunits = kv_heads * p.q_tiles;
   qlaunch::query_kernel<<<qunits < st->sms ? qunits : st->sms, qlaunch::kThreads,
-                          qlaunch::kSmemBytes, stream>>>(tmQ, tmDO, tmK, tmVT, p);
+                          qlaunch::kSmemBytes, stream>>>(tmQ, tmDO, tmO, tmK, tmVT, p);
   klaunch::key_kernel<<<kunits < st->sms ? kunits : st->sms, klaunch::kThreads,
                         klaunch::kSmemBytes, stream>>>(tmK, tmVT, tmQ, tmDO, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
