@@ -4,15 +4,15 @@
 // transpose done in the product's epilogue (the page ".../Coppelius/Build/Graph.alpha"
 // runs these as the QKV product, then "qk-rope", then "value-transpose").
 //
-// Persistent clusters of two CTAs (one per SM) walk pairs of output tiles:
-// tokens 256 m' .. +255 (128 per CTA) x outputs 192 n .. +191 (three heads;
-// 1024 tiles fill seven waves of 152 SMs to 96 %, where four-head tiles filled
-// six to 84 %).  In each CTA warp 0 (one lane) streams 64-wide slices of its X
-// tile and half of the shared W slice through a five-stage TMA ring, the W
-// half multicast to both CTAs of the pair, so each SM reads 28 KiB instead of
-// 40 KiB per slice from L2; warp 1 issues the tcgen05 MMAs (M = 128, N = 192,
-// K = 16) into one of two tensor-memory accumulators and releases each stage
-// to both CTAs;
+// A persistent grid (one CTA per SM) walks the output tiles in pairs: tokens
+// 256 m' .. +255 (two 128-token tiles, taken by CTAs 2i and 2i + 1) x outputs
+// 192 n .. +191 (three heads; 1024 tiles fill seven waves of 152 SMs to 96 %,
+// where four-head tiles filled six to 84 %).  The two CTAs of a pair read the
+// same W slice at about the same time, so the second read is served by L2.  In
+// each CTA warp 0 (one lane) streams 64-wide slices of its X tile and of the W
+// slice through a five-stage TMA ring, with plain loads into its own shared
+// memory; warp 1 issues the tcgen05 MMAs (M = 128, N = 192, K = 16) into one of
+// two tensor-memory accumulators and releases each stage once they have read it;
 // warps 2-5 (one token per thread) take a finished accumulator, rotate the
 // query and key heads' pairs in binary32, round to binary16 and write Q and K
 // rows and V^T columns, while the next tile accumulates in the other buffer.
@@ -101,20 +101,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ void load_role(const CUtensorMap *tmX, const CUtensorMap *tmW, const QkvParams &p,
                           const Sync &sy, uint32_t smem) {
   const int pairs = (p.m_tiles + 1) / 2 * p.n_tiles;
-  const int rank = (int)cluster_rank();
+  const int rank = (int)(blockIdx.x & 1);
   uint32_t it = 0, issued = 0;
   for (int tp = blockIdx.x / 2; tp < pairs; tp += gridDim.x / 2) {
     const int m = 2 * (tp / p.n_tiles) + rank, n = tp % p.n_tiles;
     for (int kc = 0; kc < p.k_slices; ++kc, ++it) {
       const uint32_t s = it % kStages;
-      // both CTAs' products must have read this stage before either refills it
       if (!sy.wait(kBarEmpty + s, ((it / kStages) & 1) ^ 1, 401)) goto drain;
       const uint32_t dst = smem + s * kStageBytes;
       mbar_arrive_expect_tx(sy.bar(kBarFull + s), kStageBytes);
       issued = it + 1;
       tma_load_3d(dst, tmX, sy.bar(kBarFull + s), kc * kBK, m * kBM, 0);
-      tma_load_3d_mc(dst + kABytes + rank * (kBBytes / 2), tmW, sy.bar(kBarFull + s), kc * kBK,
-                     n * kBN + rank * (kBN / 2), 0, (uint16_t)3);
+      tma_load_3d(dst + kABytes, tmW, sy.bar(kBarFull + s), kc * kBK, n * kBN, 0);
     }
   }
   return;
@@ -142,7 +140,7 @@ __device__ void mma_role(const QkvParams &p, const Sync &sy, uint32_t smem, uint
       for (int e = 0; e < kBK / 16; ++e)
         mma_ss(tmem + kBN * b, sw128_desc(base + e * 32), sw128_desc(base + kABytes + e * 32), id,
                (kc > 0 || e > 0) ? 1u : 0u);
-      mma_commit_mc(sy.bar(kBarEmpty + s), (uint16_t)3);   // both CTAs may refill the stage
+      mma_commit(sy.bar(kBarEmpty + s));
     }
     mma_commit(sy.bar(kBarAccFull + b));
   }
@@ -159,7 +157,7 @@ __device__ void epilogue_role(const QkvParams &p, const Sync &sy, uint32_t tmem)
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const int pairs = (p.m_tiles + 1) / 2 * p.n_tiles;
   const int heads_all = p.heads + 2 * p.kv_heads;
-  const int rank = (int)cluster_rank();
+  const int rank = (int)(blockIdx.x & 1);
   uint32_t lt = 0;
   for (int tp = blockIdx.x / 2; tp < pairs; tp += gridDim.x / 2, ++lt) {
     const int m = 2 * (tp / p.n_tiles) + rank, n = tp % p.n_tiles;
@@ -213,7 +211,7 @@ __device__ void epilogue_role(const QkvParams &p, const Sync &sy, uint32_t tmem)
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     qkv_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const QkvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -228,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(sy.bar(kBarFull + i), 1);
-      mbar_init(sy.bar(kBarEmpty + i), 2);   // the two CTAs' products
+      mbar_init(sy.bar(kBarEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(sy.bar(kBarAccFull + i), 1);
@@ -244,7 +242,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem_gen + kOffTmemPtr);
   if (warp == 0) {
@@ -257,7 +254,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // no multicast copy or commit of the peer is still aimed at this CTA
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -267,7 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------- host side
 struct QkvState {
   bool ready = false;
-  int clusters = 0;   // CTA pairs that can be resident at once
+  int sms = 0;
   int *status = nullptr;
 };
 std::mutex g_qkv_mutex;
@@ -300,16 +296,7 @@ int qkv_state(QkvState **out) {
       return ATTN_ELAUNCH;
     if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
     if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(prop.multiProcessorCount & ~1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, qkv_kernel, &cfg) != cudaSuccess || clusters <= 0) {
-      cudaGetLastError();
-      clusters = prop.multiProcessorCount / 2;
-    }
-    st.clusters = clusters;
+    st.sms = prop.multiProcessorCount;
     st.ready = true;
   }
   *out = &st;
@@ -368,8 +355,7 @@ extern "C" int attn_qkv_rope(const void *x, const void *w, const float *cosines,
   int rc = qkv_state(&st);
   if (rc) return rc;
   CUtensorMap tmX, tmW;
-  // each CTA of a pair loads (and multicasts) half of the W slice: 96 rows
-  if (!encode_rows(&tmX, x, width, T, kBM) || !encode_rows(&tmW, w, width, n_out, kBN / 2))
+  if (!encode_rows(&tmX, x, width, T, kBM) || !encode_rows(&tmW, w, width, n_out, kBN))
     return ATTN_ELAUNCH;
   QkvParams p;
   p.T = T;
@@ -387,7 +373,9 @@ extern "C" int attn_qkv_rope(const void *x, const void *w, const float *cosines,
   p.vT = static_cast<__half *>(vT);
   p.status = st->status;
   const int pairs = (p.m_tiles + 1) / 2 * p.n_tiles;
-  const int grid = 2 * (pairs < st->clusters ? pairs : st->clusters);
+  // an even grid: CTAs 2i and 2i + 1 take the two token tiles of a pair
+  const int slots = st->sms / 2;
+  const int grid = 2 * (pairs < slots ? pairs : slots);
   qkv_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmX, tmW, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;

@@ -93,34 +93,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA load multicast to the CTAs in `mask` (same shared-memory offset and barrier offset in each).
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
-                                               int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
-      : "memory");
-}
-// Arrive once on `bar` in every CTA of `mask` when this thread's prior MMAs are complete.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-      ::"r"(bar), "h"(mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 // Allocates `ncols` TMEM columns (whole warp); the base address lands in smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
