@@ -129,12 +129,15 @@ int attn_last_device_status(cudaStream_t stream);
  * cudaFree or other allocating routine.
  *
  * Arguments, layouts, admission checks and results are those of attn_fwd.
- * status: NULL, or a host or device pointer that receives (ordered on
- *   `stream`) the kernel's status word: 0 if every wait inside the kernel
- *   completed, non-zero if one gave up (then o and lse are not valid).
+ * status: NULL, or a pointer to device, managed or page-locked host memory
+ *   that receives (ordered on `stream`) the kernel's status word: 0 if every
+ *   wait inside the kernel completed, non-zero if one gave up (then o and lse
+ *   are not valid).  A pointer to pageable host memory returns ATTN_EINVAL.
  *
- * The scratch this kernel needs does not depend on the shape (192 bytes); the
- * call returns ATTN_EINVAL if it ever exceeded the array's 256 bytes.
+ * The scratch this kernel needs does not depend on the shape: it fills the
+ * whole 256-byte array (the status word at word 0, words 1-31 unused, the 16
+ * counter slots of two words at words 32-63), checked when the library is
+ * compiled.
  * The first call on each device looks up the array's device address and
  * sets the kernel's shared-memory attribute: make that first call before any
  * stream capture.  Each call clears the status word and its counter slot

@@ -1,57 +1,105 @@
 """attn_fwd_noalloc through the C ABI: the entry point for callers that cannot
 allocate device memory (memory-planned runtimes, fixed device-memory quotas,
 loops that cannot take cudaMalloc's implicit synchronisation).  Its scratch,
-the kernel's status word, lives in a fixed array inside the library.
+the kernel's status word and tile-scheduler counters, lives in a fixed array
+inside the library.
 
-Two calls in a row must each match attn_fwd's output within the parity
-tolerances (max |dO| <= 4e-3, max |dLSE| <= 1e-3) and report a clean status.
+The check runs in a fresh child process, so no earlier call of attn_fwd has
+already made the allocation the entry point must never make:
+  * two no-alloc calls in a row each match attn_fwd's output within the parity
+    tolerances (max |dO| <= 4e-3, max |dLSE| <= 1e-3) and report a clean status;
+  * the device's free memory is the same before and after a no-alloc call;
+  * attn_fwd's first call, made afterwards, does lower it (its per-device
+    scratch block), which shows the measurement can see such an allocation and
+    that the no-alloc calls did not make it on attn_fwd's behalf;
+  * a pageable host status pointer is rejected before anything is queued.
 This file is collected last so a failure here cannot hide another test.
 """
-import ctypes
+import json
+import os
+import subprocess
+import sys
 
-import numpy as np
 import pytest
 import torch
 
-import synthetic
-import transformer_causal_gqa_gb300 as tcg
 from transformer_causal_gqa_gb300 import build as tcg_build
 
 pytestmark = pytest.mark.gpu
 
 TOL_O = 4e-3
 TOL_LSE = 1e-3
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import ctypes, json, sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+import synthetic
+import transformer_causal_gqa_gb300 as tcg
+
+lib = tcg.load_library()
+dev = torch.device("cuda:0")
+w = synthetic.custom(1088, 8, 2, seed=4242)
+q, k, vT = (torch.from_numpy(x).to(dev) for x in synthetic.make_inputs(w))
+c = synthetic.scale_c()
+T, H, G = w.T, w.heads, w.kv_heads
+outs = [(torch.full((T, H * 64), float("nan"), dtype=torch.float16, device=dev),
+         torch.full((H, T), float("nan"), dtype=torch.float32, device=dev)) for _ in range(3)]
+status = torch.full((2,), -7, dtype=torch.int32).pin_memory()
+pageable = (ctypes.c_int * 1)(-7)
+stream = torch.cuda.current_stream()
+vp = ctypes.c_void_p
+torch.cuda.synchronize()
+
+def noalloc(o, lse, st):
+    return lib.attn_fwd_noalloc(vp(q.data_ptr()), vp(k.data_ptr()), vp(vT.data_ptr()),
+                                vp(o.data_ptr()), vp(lse.data_ptr()), T, H, G, c,
+                                st, vp(stream.cuda_stream))
+
+res = {}
+res["rc0"] = noalloc(*outs[0], vp(status.data_ptr()))
+stream.synchronize()
+res["status0"] = int(status[0])
+free_before = torch.cuda.mem_get_info()[0]
+res["rc1"] = noalloc(*outs[1], vp(status.data_ptr() + 4))
+stream.synchronize()
+res["status1"] = int(status[1])
+free_after = torch.cuda.mem_get_info()[0]
+res["rc_pageable"] = noalloc(*outs[1], ctypes.cast(pageable, vp))
+res["free_delta_noalloc"] = free_before - free_after
+o_ref, l_ref = outs[2]
+res["rc_ref"] = lib.attn_fwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(vT.data_ptr()),
+                             vp(o_ref.data_ptr()), vp(l_ref.data_ptr()), T, H, G, c,
+                             vp(stream.cuda_stream))
+res["status_ref"] = tcg.last_device_status()
+res["free_delta_attn_fwd"] = free_after - torch.cuda.mem_get_info()[0]
+for i in range(2):
+    o, lse = outs[i]
+    res[f"d_o{i}"] = (o.double() - o_ref.double()).abs().max().item()
+    res[f"d_l{i}"] = (lse.double() - l_ref.double()).abs().max().item()
+    res[f"finite{i}"] = bool(torch.isfinite(o).all().item() and torch.isfinite(lse).all().item())
+print("RESULT " + json.dumps(res))
+"""
 
 
-def test_noalloc_matches_attn_fwd_twice():
+def test_noalloc_allocates_nothing_and_matches_attn_fwd_twice():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     tcg_build.build()
-    lib = tcg.load_library()
-    dev = torch.device("cuda:0")
-    w = synthetic.custom(1088, 8, 2, seed=4242)
-    q, k, vT = (torch.from_numpy(x).to(dev) for x in synthetic.make_inputs(w))
-    c = synthetic.scale_c()
-    T, H, G = w.T, w.heads, w.kv_heads
-
-    o_ref = torch.empty((T, H * 64), dtype=torch.float16, device=dev)
-    l_ref = torch.empty((H, T), dtype=torch.float32, device=dev)
-    tcg.attn_fwd(q, k, vT, o_ref, l_ref, T, H, G, c)
-    assert tcg.last_device_status() == tcg.ATTN_OK
-
-    stream = torch.cuda.current_stream()
-    status = torch.full((1,), -7, dtype=torch.int32).pin_memory()
-    for _ in range(2):
-        o = torch.full((T, H * 64), float("nan"), dtype=torch.float16, device=dev)
-        lse = torch.full((H, T), float("nan"), dtype=torch.float32, device=dev)
-        vp = ctypes.c_void_p
-        rc = lib.attn_fwd_noalloc(vp(q.data_ptr()), vp(k.data_ptr()), vp(vT.data_ptr()),
-                                  vp(o.data_ptr()), vp(lse.data_ptr()), T, H, G, c,
-                                  vp(status.data_ptr()), vp(stream.cuda_stream))
-        assert rc == tcg.ATTN_OK, tcg.status_string(rc)
-        stream.synchronize()
-        assert int(status[0]) == 0
-        d_o = (o.double() - o_ref.double()).abs().max().item()
-        d_l = (lse.double() - l_ref.double()).abs().max().item()
-        assert d_o <= TOL_O and d_l <= TOL_LSE, (d_o, d_l)
-        assert np.isfinite(o.float().cpu().numpy()).all()
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES=os.environ.get("CUDA_VISIBLE_DEVICES", "0"))
+    run = subprocess.run([sys.executable, "-c", CHILD, ROOT], capture_output=True, text=True,
+                         timeout=600, env=env)
+    lines = [ln for ln in run.stdout.splitlines() if ln.startswith("RESULT ")]
+    assert run.returncode == 0 and lines, run.stdout[-2000:] + run.stderr[-4000:]
+    res = json.loads(lines[-1][len("RESULT "):])
+    assert res["rc0"] == 0 and res["rc1"] == 0, res
+    assert res["status0"] == 0 and res["status1"] == 0, res
+    assert res["rc_ref"] == 0 and res["status_ref"] == 0, res
+    assert res["rc_pageable"] == -1, res          # ATTN_EINVAL
+    assert res["free_delta_noalloc"] == 0, res
+    assert res["free_delta_attn_fwd"] > 0, res
+    for i in range(2):
+        assert res[f"finite{i}"], res
+        assert res[f"d_o{i}"] <= TOL_O and res[f"d_l{i}"] <= TOL_LSE, res

@@ -170,10 +170,11 @@ def attn_fwd_host(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
 
 def attn_fwd_noalloc(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: float,
                      status=None, stream=None) -> None:
-    """attn_fwd without any device allocation: the kernel's status word lives in a
-    fixed array inside the library.  ``status``: None, or a 1-element int32 tensor
-    (host or CUDA) that receives the word (0 = every kernel wait completed) in
-    stream order.  Calls that overlap on the GPU share the word."""
+    """attn_fwd without any device allocation: the kernel's scratch (its status word
+    and tile-scheduler counters) lives in a fixed array inside the library.
+    ``status``: None, or a 1-element int32 tensor (CUDA, or pinned host memory)
+    that receives the word (0 = every kernel wait completed) in stream order.
+    Calls that overlap on the GPU share the array."""
     import torch
     _check_tensor("q", q, torch.float16, (heads, T, HEAD_DIM))
     _check_tensor("k", k, torch.float16, (kv_heads, T, HEAD_DIM))

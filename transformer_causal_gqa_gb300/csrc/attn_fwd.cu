@@ -928,12 +928,14 @@ extern "C" int attn_last_device_status(cudaStream_t stream) {
 // fixed array compiled into this library instead of a cudaMalloc'd word.
 
 // 256 bytes (64 words), held by every GPU that loads this library until the
-// process exits: the status word at [0] and 16 work-counter slots of two words
-// from [32].  Host code must not use this name as a device address: it gets
-// the address from cudaGetSymbolAddress.
+// process exits: the status word at [0], words [1, 32) unused, and 16
+// work-counter slots of two words at [32, 64).  Host code must not use this
+// name as a device address: it gets the address from cudaGetSymbolAddress.
 constexpr int kNoAllocSchedSlots = 16;
 constexpr int kNoAllocScratchInts = kScratchSched + 2 * kNoAllocSchedSlots;
 static __device__ __align__(256) int g_noalloc_scratch[64];
+static_assert(kNoAllocScratchInts * sizeof(int) <= sizeof(g_noalloc_scratch),
+              "the kernel's scratch must fit the fixed array");
 
 namespace {
 
@@ -993,9 +995,17 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, vo
                                 cudaStream_t stream) {
   int rc = check_args(q, k, vT, o, lse, T, heads, kv_heads, c);
   if (rc) return rc;
-  // the scratch this kernel needs is the same for every shape
-  const size_t scratch_needed = kNoAllocScratchInts * sizeof(int);
-  if (scratch_needed > sizeof(g_noalloc_scratch)) return ATTN_EINVAL;
+  if (status) {
+    // the status copy is stream-ordered: pageable host memory would make it
+    // synchronous (and it cannot be captured), so only device, managed or
+    // page-locked host memory is accepted
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, status) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_EINVAL;
+    }
+    if (attr.type == cudaMemoryTypeUnregistered) return ATTN_EINVAL;
+  }
   NoAllocState *st = nullptr;
   if ((rc = noalloc_state(&st))) return rc;
   CUtensorMap tm[3];
