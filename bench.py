@@ -14,6 +14,16 @@ in it.  Each launch is timed with CUDA events on the launching stream.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
   python bench.py --pass backward ...    # the backward pass instead (see below)
+  python bench.py --all-configs          # one line per workload: timing + full parity
+
+The --all-configs mode (one GPU) prints one JSON line per workload of the
+benchmark list: the kernel's time (CUDA events; the three small workloads as
+20 event pairs around 200 back-to-back launches each, the two large ones as
+launches with L2 flushed between them), causal TFLOP/s and fraction of the
+peaks, max |dO| and max |dLSE| of one launch against the fp64 oracle on every
+element, the oracle's wall time, its thread count, the host's hardware thread
+count and CPU model.  It is a record of every configuration, not the contract
+line.
 
 The materialised mode (--pass materialised) times one attn_fwd_materialised
 call per step: the same forward through a binary32 scores plane and a
@@ -64,6 +74,8 @@ METRIC_MAT = "materialised causal attn fwd TFLOP/s (scores + probability planes)
 METRIC_QKV = "fused QKV producer (product + rotary + V transpose) TFLOP/s and % of fp16 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
+# NVIDIA's nominal dense (no 2:4 sparsity) fp16/bf16 tensor rate of one GB300
+DATASHEET_FP16_TFLOPS = 2250.0
 FLUSH_BYTES = 512 << 20
 KERNEL_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_fwd.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_t8192_h32_kv8.md")
@@ -85,6 +97,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=120.0,
                     help="CPU seconds the reference arm spends over warm-up and timed steps")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one line per workload: kernel time and full-oracle parity")
     ap.add_argument("--pass", dest="which",
                     choices=["forward", "backward", "materialised", "producer"], default="forward")
     return ap.parse_args()
@@ -363,6 +377,11 @@ def run_gb300(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": peak_note,
+                         "datasheet": {"peak": DATASHEET_FP16_TFLOPS,
+                                       "frac": achieved / DATASHEET_FP16_TFLOPS,
+                                       "source": "NVIDIA GB300 nominal dense fp16/bf16 rate"},
+                         "ncu_tensor_pipe_active_pct": kernel_traffic(
+                             key="tensor_pipe_active_pct"),
                          "kernel": "attn_fwd_kernel",
                          "launch_ms": {"mean": avg_launch_s * 1e3,
                                        "median": statistics.median(per_launch_ms),
@@ -576,6 +595,9 @@ def run_gb300_backward(args):
                          "traffic": kernel_traffic(BWD_TRAFFIC_SUMMARY, BWD_SOURCE,
                                                    "traffic_bytes_per_call"),
                          "peak_source": peak_note,
+                         "datasheet": {"peak": DATASHEET_FP16_TFLOPS,
+                                       "frac": achieved / DATASHEET_FP16_TFLOPS,
+                                       "source": "NVIDIA GB300 nominal dense fp16/bf16 rate"},
                          "kernel": "attn_bwd call (query_kernel then key_kernel)",
                          "launch_ms": {"mean": avg_s * 1e3,
                                        "median": statistics.median(per_call_ms),
@@ -929,6 +951,9 @@ def run_gb300_producer(args):
                          "frac": achieved / peak,
                          "traffic": kernel_traffic(QKV_TRAFFIC_SUMMARY, QKV_SOURCE),
                          "peak_source": peak_note, "kernel": "qkv_kernel",
+                         "datasheet": {"peak": DATASHEET_FP16_TFLOPS,
+                                       "frac": achieved / DATASHEET_FP16_TFLOPS,
+                                       "source": "NVIDIA GB300 nominal dense fp16/bf16 rate"},
                          "launch_ms": {"mean": avg_s * 1e3, "median": statistics.median(per_ms),
                                        "min": min(per_ms)}},
             "e2e": {"value": world * E * flops / e2e_s / 1e12, "unit": UNIT,
@@ -984,9 +1009,110 @@ def run_reference_producer(args):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
+# ----------------------------------------------------------------------------- every workload
+def cpu_model():
+    """The host CPU's model name, from /proc/cpuinfo or lscpu."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
+def run_all_configs(args):
+    import torch
+
+    import oracle
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    tcg_build.build()
+    tcg.load_library()
+    c = synthetic.scale_c()
+    peak, peak_note = measured_peak()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    host = {"cpu_model": cpu_model(), "hardware_concurrency": os.cpu_count(),
+            "oracle_threads": oracle.max_threads()}
+    for w in synthetic.WORKLOADS.values():
+        inputs = synthetic.make_inputs(w)
+        q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
+        o = torch.full((w.T, w.heads * 64), float("nan"), dtype=torch.float16, device=dev)
+        lse = torch.full((w.heads, w.T), float("nan"), dtype=torch.float32, device=dev)
+
+        def step():
+            tcg.attn_fwd(q, k, vT, o, lse, w.T, w.heads, w.kv_heads, c, stream)
+
+        step()
+        if tcg.last_device_status(stream) != tcg.ATTN_OK:
+            raise RuntimeError(f"{w.name}: device status after the parity launch is not OK")
+        o_gpu = o.cpu().numpy().astype(np.float64)
+        l_gpu = lse.cpu().numpy().astype(np.float64)
+        for _ in range(max(3, args.warmup)):
+            step()
+        small = w.T <= 2048
+        per_pair = 200 if small else 1
+        pairs = 20 if small else max(20, min(args.steps, 200))
+        sampler = ClockSampler(gpu_uuid())
+        sampler.start()
+        times = []
+        torch.cuda.synchronize()
+        for _ in range(pairs):
+            if not small:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(per_pair):
+                step()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        if tcg.last_device_status(stream) != tcg.ATTN_OK:
+            raise RuntimeError(f"{w.name}: device status after timing is not OK")
+        ms = [a.elapsed_time(b) / per_pair for a, b in times]
+        t0 = time.perf_counter()
+        o_ref, l_ref = oracle.attn_fwd(*inputs, w.T, w.heads, w.kv_heads, c)
+        oracle_s = time.perf_counter() - t0
+        d_o = float(np.abs(o_gpu - o_ref).max())
+        d_l = float(np.abs(l_gpu - l_ref).max())
+        med = statistics.median(ms)
+        tflops = w.causal_flops / (med / 1e3) / 1e12
+        print(json.dumps({
+            "mode": "all-configs", "workload": w.name, "T": w.T, "heads": w.heads,
+            "kv_heads": w.kv_heads, "gpu_ms_median": med, "gpu_ms_mean": statistics.fmean(ms),
+            "gpu_ms_min": min(ms), "event_pairs": pairs, "launches_per_event_pair": per_pair,
+            "l2": ("warm: back-to-back launches inside each event pair" if small else
+                   "flushed before each launch (512 MiB write)"),
+            "tflops": tflops, "frac_of_measured_peak": tflops / peak, "peak": peak,
+            "peak_source": peak_note, "frac_of_datasheet_fp16": tflops / DATASHEET_FP16_TFLOPS,
+            "max_abs_dO": d_o, "max_abs_dLSE": d_l, "tol_dO": 4e-3, "tol_dLSE": 1e-3,
+            "parity": "pass" if (d_o <= 4e-3 and d_l <= 1e-3) else "FAIL",
+            "oracle_s": oracle_s, "oracle_rows": "every row", **host,
+            "oracle_gflops": w.causal_flops / oracle_s / 1e9, "clocks": clocks,
+        }), flush=True)
+        del q, k, vT, o, lse, o_ref, l_ref, o_gpu, l_gpu
+        torch.cuda.empty_cache()
+
 
 def main():
     args = parse_args()
+    if args.all_configs:
+        if args.impl == "reference":
+            raise SystemExit("--all-configs times the GPU kernel; the oracle is timed inside it")
+        run_all_configs(args)
+        return
     if args.which == "producer":
         (run_reference_producer if args.impl == "reference" else run_gb300_producer)(args)
     elif args.which == "materialised":
