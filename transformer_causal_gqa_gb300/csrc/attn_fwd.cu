@@ -375,10 +375,8 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
         const uint32_t kslot = (pos + 2 * j) % kStages;
         const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
         const uint32_t qbase = smem + kOffQ + (qb * 2 + s) * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_ss(tmem + kColS + 128u * s, sw128_desc(qbase + kk * 32), sw128_desc(kbase + kk * 32),
-                 idS, kk > 0 ? 1u : 0u);
+        // the four MMAs of S_s(j) under one election (issued back to back)
+        mma_ss_k64(tmem + kColS + 128u * s, sw128_desc(qbase), sw128_desc(kbase), idS);
         mma_commit(sy.bar(kBarSFull + s));
         if (s) { ++s_issued1; j1 = j + 1; } else { ++s_issued0; j0 = j + 1; }
         // K(j) is released once every subtile that reads it has its S issued
