@@ -162,6 +162,22 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, floa
  */
 int attn_test_inject_stall(void);
 
+/*
+ * attn_test_set_split_mode -- test hook choosing the forward kernel's mode.
+ *
+ * The source pages have no counterpart of this entry point.  attn_fwd (and
+ * attn_fwd_host, attn_fwd_noalloc) run short problems -- fewer 256-row units
+ * (heads * ceil(T / 256)) than the device has SMs -- in a split mode: a work
+ * unit is 128 query rows whose key tiles are shared out between the kernel's
+ * two softmax warpgroups, and the two partial results of every row are merged
+ * at the end.  Longer problems run in the normal mode (256-row units, both
+ * warpgroups over all key tiles of their own 128 rows).  Both modes compute
+ * the same quantities.  mode: -1 chooses by size (the default), 0 forces the
+ * normal mode, 1 the split mode, for every later call in this process.
+ * Returns ATTN_OK, or ATTN_EINVAL for any other mode.
+ */
+int attn_test_set_split_mode(int mode);
+
 /* A static, human-readable name for a status code. */
 const char *attn_status_string(int status);
 

@@ -32,6 +32,14 @@ def lib():
     return tcg.load_library()
 
 
+@pytest.fixture
+def mode(request):
+    """Forces the forward kernel's mode (0 normal, 1 split) for one test."""
+    tcg.set_split_mode(request.param)
+    yield request.param
+    tcg.set_split_mode(-1)
+
+
 def run_gpu(q, k, vT, T, H, G, c, stream=None):
     dev = torch.device("cuda:0")
     qd, kd, vd = (torch.from_numpy(x).to(dev) for x in (q, k, vT))
@@ -60,11 +68,20 @@ def test_workload_every_element(name):
     compare_full(synthetic.WORKLOADS[name])
 
 
-# ragged tails: T mod 256 in {64, 128, 192, 0}; groups 1, 2, 4, 8
+# ragged tails: T mod 256 in {64, 128, 192, 0}; groups 1, 2, 4, 8; both modes of the
+# kernel (short problems run split by default: the two subtiles share out a 128-row
+# unit's key tiles and merge; the normal mode gives each subtile its own 128 rows)
+@pytest.mark.parametrize("mode", [0, 1], indirect=True)
 @pytest.mark.parametrize("T", [64, 192, 320, 384, 448, 640, 1088])
 @pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1)])
-def test_shapes_every_element(T, H, G):
+def test_shapes_every_element(mode, T, H, G):
     compare_full(synthetic.custom(T, H, G, seed=T * 100 + H * 10 + G))
+
+
+@pytest.mark.parametrize("mode", [0, 1], indirect=True)
+@pytest.mark.parametrize("name", ["t128_h4_kv2", "t1024_h12_kv12_mha", "t2048_h16_kv4_peaked"])
+def test_small_workloads_both_modes(mode, name):
+    compare_full(synthetic.WORKLOADS[name])
 
 
 def test_outlier_keys_small():
@@ -171,8 +188,9 @@ def compare_arrays(q, k, vT, T, H, G):
     assert d_l <= TOL_LSE, f"max |dLSE| = {d_l}"
 
 
+@pytest.mark.parametrize("mode", [0, 1], indirect=True)
 @pytest.mark.parametrize("jump", [6.0, 12.0, 14.0, 16.0, 40.0, 120.0, 200.0])
-def test_late_score_jump(jump):
+def test_late_score_jump(mode, jump):
     """A key late in the sequence whose score exceeds every earlier one by `jump`
     (base-2 units) for every query row after it.  Each row's weight for that key
     is 2^(jump + d) against its reference maximum, d >= 0 the row's own gap to
@@ -202,8 +220,9 @@ def test_late_score_jump(jump):
     compare_arrays(q16, k16, vT, T, H, G)
 
 
+@pytest.mark.parametrize("mode", [0, 1], indirect=True)
 @pytest.mark.parametrize("rise", [1.0, 3.0, 9.0])
-def test_tile_wide_rise(rise):
+def test_tile_wide_rise(mode, rise):
     """Every key of one tile scores `rise` above the largest earlier score, for
     every query row after the tile: 128 equal weights of at least 2^rise, tied at
     the tile's maximum.  With rises 1 and 3 most rows keep their reference (row

@@ -36,6 +36,7 @@ ATTN_ETIMEOUT = -6
 # every symbol the headers under include/ declare
 EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_last_device_status", "attn_fwd_noalloc", "attn_test_inject_stall",
+            "attn_test_set_split_mode",
             "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
             "attn_bwd_last_device_status", "attn_bwd_test_inject_stall", "attn_fwd_materialised",
             "attn_materialised_workspace_bytes", "attn_materialised_last_device_status",
@@ -77,6 +78,8 @@ def load_library():
     lib.attn_fwd_noalloc.restype = i
     lib.attn_test_inject_stall.argtypes = []
     lib.attn_test_inject_stall.restype = i
+    lib.attn_test_set_split_mode.argtypes = [i]
+    lib.attn_test_set_split_mode.restype = i
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, f, f, vp, sz, vp]
@@ -189,6 +192,15 @@ def attn_fwd_noalloc(q, k, vT, o, lse, T: int, heads: int, kv_heads: int, c: flo
                                          _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
+
+
+def set_split_mode(mode: int) -> None:
+    """Test hook: -1 lets attn_fwd choose its mode by size, 0 forces the normal mode,
+    1 the split mode (short problems' key tiles shared out between the two softmax
+    warpgroups of a CTA).  Affects every later forward call in this process."""
+    rc = load_library().attn_test_set_split_mode(int(mode))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_test_set_split_mode")
 
 
 def last_device_status(stream=None) -> int:

@@ -35,6 +35,13 @@
 //   are those of the page's recurrence with another choice of m; O / l and
 //   m + log2 l do not depend on that choice.
 //
+// Short problems (fewer 256-row units than SMs) run in a split mode instead: a
+// unit is 128 query rows, subtile 0 takes the first half of its key tiles and
+// subtile 1 the second half (with the diagonal), both against the same Q tile,
+// and at the end subtile 1 merges the two partial (m, l, O) of each row --
+// the page's merge rule applied across the two halves -- and writes O / l and
+// m + log2 l.  The longest chain of key tiles is then half as long.
+//
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records
 // ATTN_ETIMEOUT in a device status word, drains what it has in flight, frees
 // its tensor memory and exits.
@@ -88,7 +95,9 @@ constexpr int kBarPvDone = kBarPFull + 2;       // + subtile: O_s += P_s V compl
 constexpr int kBarUnitFull = kBarPvDone + 2;    // + queue slot: a unit id published
 constexpr int kBarUnitEmpty = kBarUnitFull + kUnitSlots;  // + queue slot: read by every consumer
 constexpr int kBarDrain = kBarUnitEmpty + kUnitSlots;     // + MMA warp (0..2): its own drain on abort
-constexpr int kNumBars = kBarDrain + 3;
+constexpr int kBarMergeReady = kBarDrain + 3;   // split mode: subtile 0's partial (m, l, O) is ready
+constexpr int kBarMergeDone = kBarMergeReady + 1;  // split mode: subtile 1 has read it
+constexpr int kNumBars = kBarMergeDone + 1;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                               // 2 buffers x 2 subtiles
@@ -97,7 +106,8 @@ constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
 constexpr uint32_t kOffUnits = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffTmemPtr = kOffUnits + kUnitSlots * 4;
 constexpr uint32_t kOffAbort = kOffTmemPtr + 4;
-constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kOffMerge = (kOffAbort + 4 + 15) & ~15u;   // split mode: m and l of 128 rows
+constexpr uint32_t kSmemUsed = kOffMerge + 2 * kBlockM * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far beyond any legitimate wait
@@ -113,7 +123,7 @@ struct Params {
   int T;
   int heads;
   int group;          // query heads per K/V head
-  int row_blocks;     // ceil(T / 256)
+  int row_blocks;     // ceil(T / 256), or ceil(T / 128) in split mode
   int units;          // heads * row_blocks
   float c;
   __half *o;
@@ -126,20 +136,52 @@ struct Unit {
   int h, g, b;        // query head, K/V head, row block
   int row0;           // first query row
   int n0, n1;         // key tiles visited by subtile 0 and subtile 1
+  // split mode only:
+  int k1;             // key tile of subtile 1's first step (n0)
+  int diag0, diag1;   // step of each subtile that meets the diagonal (-1: none)
+  int ring;           // ring positions the unit's K and V^T tiles take
 };
 
 // Unit u in order of decreasing cost: the latest row blocks (most key tiles) first.
+// Normal mode: 256 rows, subtile s holds rows 128 s .. +127 and visits tiles 0 ..
+// its diagonal; both read every K, V^T tile.  Split mode: 128 rows read by both
+// subtiles; of the n key tiles 0 .. diagonal, subtile 0 visits the first n / 2
+// and subtile 1 the rest; each tile is read by one subtile.
+template <bool kSplit>
 __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
   Unit w;
   const int rb = u / p.heads;
   w.h = u - rb * p.heads;
   w.b = p.row_blocks - 1 - rb;
   w.g = w.h / p.group;
-  w.row0 = w.b * kUnitRows;
-  const int end = min(p.T, w.row0 + kUnitRows);
-  w.n0 = 2 * w.b + 1;                   // subtile 0: tiles 0 .. its diagonal 2b
-  w.n1 = (end + kBlockN - 1) / kBlockN; // subtile 1: through 2b+1, or 2b when it holds no row < T
+  if (!kSplit) {
+    w.row0 = w.b * kUnitRows;
+    const int end = min(p.T, w.row0 + kUnitRows);
+    w.n0 = 2 * w.b + 1;                   // subtile 0: tiles 0 .. its diagonal 2b
+    w.n1 = (end + kBlockN - 1) / kBlockN; // subtile 1: through 2b+1, or 2b when it holds no row < T
+    // k1, diag0, diag1 and ring serve the split mode only (the normal mode
+    // uses 0, 2b, 2b+1 and 2 n1 directly)
+    w.k1 = w.diag0 = w.diag1 = w.ring = 0;
+  } else {
+    w.row0 = w.b * kBlockM;
+    const int n = w.b + 1;
+    w.n0 = n / 2;
+    w.n1 = n - w.n0;
+    w.k1 = w.n0;
+    w.diag0 = -1;
+    w.diag1 = w.n1 - 1;
+    w.ring = 2 * n;
+  }
   return w;
+}
+
+// Place of step j of subtile s among the unit's K, V^T tile pairs in the ring:
+// normal mode, pair j (shared by both subtiles); split mode, the two subtiles'
+// steps alternate while both have steps left, then subtile 1's remaining ones.
+template <bool kSplit>
+__device__ __forceinline__ int pair_of(const Unit &w, int s, int j) {
+  if (!kSplit) return j;
+  return j < w.n0 ? 2 * j + s : w.n0 + j;
 }
 
 struct Sync {
@@ -251,7 +293,7 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float b) {
 // them to the CTA's unit queue; for each, loads the two Q subtiles into the
 // unit's Q buffer, then K(j), V^T(j) for j = 0 .. n1-1 through the ring.
 // kStallHook (test builds of the launch only): CTA 0 skips its first K tile, so a wait runs out.
-template <bool kStallHook>
+template <bool kStallHook, bool kSplit>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const Params &p, const Sync &sy, uint32_t smem) {
   uint32_t pos = 0;         // running ring position (K and V^T tiles alternate)
@@ -265,22 +307,26 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
     sy.units[slot] = u;
     mbar_arrive(sy.bar(kBarUnitFull + slot));
     if (u < 0) break;
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<kSplit>(u, p);
     const int qb = k & 1;
     if (!sy.wait(kBarQEmpty + qb, ((k >> 1) & 1) ^ 1, 1)) goto drain;
     ++q_issued;
     const uint32_t qdst = smem + kOffQ + qb * 2 * kTileBytes;
-    mbar_arrive_expect_tx(sy.bar(kBarQFull + qb), 2 * kTileBytes);
+    // split mode: one Q tile, read by both subtiles
+    mbar_arrive_expect_tx(sy.bar(kBarQFull + qb), (kSplit ? 1 : 2) * kTileBytes);
     tma_load_3d(qdst, tmQ, sy.bar(kBarQFull + qb), 0, w.row0, w.h);
-    tma_load_3d(qdst + kTileBytes, tmQ, sy.bar(kBarQFull + qb), 0, w.row0 + kBlockM, w.h);
-    for (int j = 0; j < w.n1; ++j) {
+    if (!kSplit) tma_load_3d(qdst + kTileBytes, tmQ, sy.bar(kBarQFull + qb), 0, w.row0 + kBlockM, w.h);
+    for (int jp = 0; jp < (kSplit ? w.ring / 2 : w.n1); ++jp) {
+      // the key tile of pair jp
+      int j = jp;
+      if (kSplit) j = jp < 2 * w.n0 ? (jp & 1 ? w.k1 : 0) + (jp >> 1) : jp;
       for (int kv = 0; kv < 2; ++kv, ++pos) {
         const uint32_t rs = pos % kStages;
         if (!sy.wait(kBarKvEmpty + rs, ((pos / kStages) & 1) ^ 1, 2)) goto drain;
         const uint32_t dst = smem + kOffRing + rs * kTileBytes;
         const uint32_t full = sy.bar(kBarKvFull + rs);
         pos_issued = pos + 1;
-        if (kStallHook && blockIdx.x == 0 && k == 0 && j == 0 && kv == 0)
+        if (kStallHook && blockIdx.x == 0 && k == 0 && jp == 0 && kv == 0)
           continue;  // test hook: this K tile never arrives
         mbar_arrive_expect_tx(full, kTileBytes);
         if (kv == 0) {
@@ -324,6 +370,7 @@ drain:
 // both subtiles' S became ready together and their softmax warpgroups ran in
 // lockstep, meeting on the SFU; served this way, one pick every ~1000 cycles
 // keeps them about half a tile apart.
+template <bool kSplit>
 __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kBlockM, kBlockN);
   uint32_t pos = 0;
@@ -333,7 +380,7 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
     if (u == -1) return;
     if (u < 0) goto drain;
     {
-      const Unit w = decode_unit(u, p);
+      const Unit w = decode_unit<kSplit>(u, p);
       const int qb = k & 1;
       if (!sy.wait_warp(kBarQFull + qb, (k >> 1) & 1, 11)) goto drain;
       tc_fence_after();
@@ -350,7 +397,7 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
           const int s = first ^ c;
           const int js = s ? j1 : j0;
           if (js >= (s ? n1 : n0)) continue;
-          const uint32_t kpos = pos + 2 * js;
+          const uint32_t kpos = pos + 2 * pair_of<kSplit>(w, s, js);
           const uint32_t sfree_parity = ((s ? s_issued1 : s_issued0) & 1) ^ 1;
           const bool ready = mbar_test_wait(sy.bar(kBarSFree + s), sfree_parity) &&
                              mbar_test_wait(sy.bar(kBarKvFull + kpos % kStages), (kpos / kStages) & 1);
@@ -372,19 +419,20 @@ __device__ void s_role(const Params &p, const Sync &sy, uint32_t smem, uint32_t 
         tc_fence_after();
         const int s = pick;
         const int j = s ? j1 : j0;
-        const uint32_t kslot = (pos + 2 * j) % kStages;
+        const uint32_t kslot = (pos + 2 * pair_of<kSplit>(w, s, j)) % kStages;
         const uint32_t kbase = smem + kOffRing + kslot * kTileBytes;
-        const uint32_t qbase = smem + kOffQ + (qb * 2 + s) * kTileBytes;
+        const uint32_t qbase = smem + kOffQ + (qb * 2 + (kSplit ? 0 : s)) * kTileBytes;
         // the four MMAs of S_s(j) under one election (issued back to back)
         mma_ss_k64(tmem + kColS + 128u * s, sw128_desc(qbase), sw128_desc(kbase), idS);
         mma_commit(sy.bar(kBarSFull + s));
         if (s) { ++s_issued1; j1 = j + 1; } else { ++s_issued0; j0 = j + 1; }
         // K(j) is released once every subtile that reads it has its S issued
-        const bool other_done = s ? (j0 > j || j >= n0) : (j1 > j || j >= n1);
+        // (split mode: it has one reader)
+        const bool other_done = kSplit || (s ? (j0 > j || j >= n0) : (j1 > j || j >= n1));
         if (other_done) mma_commit(sy.bar(kBarKvEmpty + kslot));
       }
       mma_commit(sy.bar(kBarQEmpty + qb));  // every S of this unit issued
-      pos += 2 * w.n1;
+      pos += kSplit ? w.ring : 2 * w.n1;
     }
   }
 drain:
@@ -395,6 +443,7 @@ drain:
 // P V issuer for subtile s: O_s += P_s(j) V(j) once the softmax has written P_s(j).
 // It releases every V^T tile of the unit (the barrier counts both subtiles'
 // issuers), including the one subtile 0 does not read when n1 > n0.
+template <bool kSplit>
 __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idPV = idesc_f16_f32(kBlockM, kHeadDim);
   uint32_t pos = 0;
@@ -403,10 +452,10 @@ __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, u
     const int u = sy.next_unit(k);
     if (u == -1) return;
     if (u < 0) goto drain;
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<kSplit>(u, p);
     const int n = s ? w.n1 : w.n0;
     for (int j = 0; j < n; ++j) {
-      const uint32_t vpos = pos + 2 * j + 1;
+      const uint32_t vpos = pos + 2 * pair_of<kSplit>(w, s, j) + 1;
       const uint32_t vslot = vpos % kStages;
       if (!sy.wait_warp(kBarPFull + s, pphase, 14)) goto drain;
       pphase ^= 1;
@@ -421,11 +470,12 @@ __device__ void pv_role(int s, const Params &p, const Sync &sy, uint32_t smem, u
       }
       mma_commit(sy.bar(kBarPvDone + s));
       mma_commit(sy.bar(kBarKvEmpty + vslot));
-      // a V^T tile subtile 0 does not read: subtile 1 releases it for both, after
-      // its own wait on the tile, so the arrival cannot land in the slot's previous phase
-      if (j >= w.n0) mma_commit(sy.bar(kBarKvEmpty + vslot));
+      // a V^T tile the other subtile does not read (every tile in split mode): this
+      // issuer releases it for both, after its own wait on the tile, so the arrival
+      // cannot land in the slot's previous phase
+      if (kSplit || j >= w.n0) mma_commit(sy.bar(kBarKvEmpty + vslot));
     }
-    pos += 2 * w.n1;
+    pos += kSplit ? w.ring : 2 * w.n1;
   }
 drain:
   mma_commit(sy.bar(kBarDrain + 1 + s));
@@ -434,7 +484,9 @@ drain:
 
 // ----------------------------------------------------------------------------
 // Softmax warpgroup for subtile s: thread r owns query row r (TMEM lane r).
-__device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tmem) {
+template <bool kSplit>
+__device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tmem,
+                             float *merge_ml) {
   const int r = threadIdx.x & 127;
   const bool leader = (threadIdx.x & 31) == 0;
   const uint32_t lane_base = (uint32_t)((threadIdx.x & 96)) << 16;  // warp's 32-lane slice
@@ -446,9 +498,9 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
   for (int k = 0;; ++k) {
     const int u = sy.next_unit(k);
     if (u < 0) return;
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<kSplit>(u, p);
     const int n = s ? w.n1 : w.n0;
-    const int diag = 2 * w.b + s;
+    const int diag = kSplit ? (s ? w.diag1 : w.diag0) : 2 * w.b + s;
     float m_run = -INFINITY, l_run = 0.f;
     // S_s(j+1) is tested (without blocking) right after P_s(j) is handed over; when
     // it was already complete the next tile skips its wait.  Each barrier test
@@ -532,12 +584,51 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
       s_seen = j + 1 < n && mbar_test_wait(sy.bar(kBarSFull + s), sphase);
     }
     // epilogue: O / l and m + log2 l once the last P V is done
-    if (!sy.wait_warp(kBarPvDone + s, pvphase, 22 + s)) return;
-    pvphase ^= 1;
-    tc_fence_after();
+    if (!kSplit || n > 0) {
+      if (!sy.wait_warp(kBarPvDone + s, pvphase, 22 + s)) return;
+      pvphase ^= 1;
+      tc_fence_after();
+    }
+    if (kSplit && s == 0) {
+      // split mode: hand this half's m and l to subtile 1, which merges the two
+      // halves of every row (its O is read from tensor memory by subtile 1's warps
+      // on the same lanes), and wait until it has done so before O is reused
+      merge_ml[r] = m_run;
+      merge_ml[kBlockM + r] = l_run;
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarMergeReady));
+      if (!sy.wait_warp(kBarMergeDone, k & 1, 26)) return;
+      tc_fence_after();
+      continue;
+    }
     uint32_t orow[64];
     tmem_ld_x64(tO, orow);
-    const int row = w.row0 + s * kBlockM + r;
+    if (kSplit) {
+      // merge with subtile 0's half: m = max(m0, m1), each half scaled by 2^(m_h - m)
+      if (!sy.wait_warp(kBarMergeReady, k & 1, 27)) return;
+      tc_fence_after();
+      const float m0 = merge_ml[r], l0 = merge_ml[kBlockM + r];
+      const float m = fmaxf(m0, m_run);
+      const float a0 = l0 > 0.f ? ex2(m0 - m) : 0.f;
+      const float a1 = ex2(m_run - m);
+      if (__any_sync(0xffffffffu, l0 > 0.f)) {
+        uint32_t o0[64];
+        tmem_ld_x64(tmem + lane_base + kColO, o0);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          orow[i] = __float_as_uint(fmaf(__uint_as_float(o0[i]), a0, __uint_as_float(orow[i]) * a1));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * a1);
+      }
+      l_run = l0 * a0 + l_run * a1;
+      m_run = m;
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(sy.bar(kBarMergeDone));
+    }
+    const int row = w.row0 + (kSplit ? 0 : s * kBlockM) + r;
     if (row < p.T) {
       const float inv = 1.f / l_run;
       uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((size_t)row * p.heads + w.h) * kHeadDim);
@@ -556,7 +647,7 @@ __device__ void softmax_role(int s, const Params &p, const Sync &sy, uint32_t tm
   }
 }
 
-template <bool kStallHook>
+template <bool kStallHook, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -597,6 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sy.bar(kBarUnitEmpty + i), kConsumerWarps);
     }
     for (int i = 0; i < 3; ++i) mbar_init(sy.bar(kBarDrain + i), 1);
+    mbar_init(sy.bar(kBarMergeReady), kBlockM / 32);   // subtile 0's softmax warps
+    mbar_init(sy.bar(kBarMergeDone), kBlockM / 32);    // subtile 1's softmax warps
     *sy.abort_flag = 0;
     mbar_fence_init();
   }
@@ -611,13 +704,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     // warps 0-3 take subtile 1 (the one a unit's last tile belongs to), warps 4-7 subtile 0
-    softmax_role(1 - (warp >> 2), p, sy, tmem);
+    softmax_role<kSplit>(1 - (warp >> 2), p, sy, tmem,
+                         reinterpret_cast<float *>(smem_gen + kOffMerge));
   } else if (warp == kSWarp) {
-    s_role(p, sy, smem, tmem);
+    s_role<kSplit>(p, sy, smem, tmem);
   } else if (warp == kPvWarp0 || warp == kPvWarp0 + 1) {
-    pv_role(warp - kPvWarp0, p, sy, smem, tmem);
+    pv_role<kSplit>(warp - kPvWarp0, p, sy, smem, tmem);
   } else if (warp == kLoadWarp) {
-    if (lane == 0) load_role<kStallHook>(&tmQ, &tmK, &tmV, p, sy, smem);
+    if (lane == 0) load_role<kStallHook, kSplit>(&tmQ, &tmK, &tmV, p, sy, smem);
     __syncwarp();
   }
 
@@ -648,6 +742,42 @@ int g_stall_launches = 0;
 DeviceState g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+bool set_smem_attributes() {
+  return cudaFuncSetAttribute(attn_fwd_kernel<false, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(attn_fwd_kernel<false, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(attn_fwd_kernel<true, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(attn_fwd_kernel<true, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess;
+}
+
+// test hook: -1 chooses the mode by size (split when fewer 256-row units than SMs),
+// 0 and 1 force the normal and the split mode
+int g_split_mode = -1;
+
+// Split mode for problems with fewer 256-row units than SMs: the longest chain
+// of key tiles is then what bounds the call, and splitting each unit's key
+// tiles between the two subtiles halves it.
+bool use_split(int T, int heads, int sms) {
+  int mode;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    mode = g_split_mode;
+  }
+  if (mode >= 0) return mode == 1;
+  return (long long)heads * ((T + kUnitRows - 1) / kUnitRows) < sms;
+}
+
+template <bool kStallHook>
+void launch_kernel(bool split, int grid, cudaStream_t stream, const CUtensorMap *tm, const Params &p) {
+  if (split)
+    attn_fwd_kernel<kStallHook, true><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+  else
+    attn_fwd_kernel<kStallHook, false><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+}
+
 int device_state(DeviceState **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -669,11 +799,7 @@ int device_state(DeviceState **out) {
         return ATTN_ELAUNCH;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return ATTN_ELAUNCH;
+    if (!set_smem_attributes()) return ATTN_ELAUNCH;
     if (cudaMalloc(&st.scratch, kScratchInts * sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
     if (cudaMemset(st.scratch, 0, kScratchInts * sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
     st.sms = prop.multiProcessorCount;
@@ -742,7 +868,7 @@ int check_args(const void *q, const void *k, const void *vT, const void *o, cons
 
 // Encodes the three tensor maps and fills the kernel parameters (all but the scratch).
 bool prepare(const void *q, const void *k, const void *vT, void *o, float *lse, int T, int heads,
-             int kv_heads, float c, CUtensorMap *tm, Params *p) {
+             int kv_heads, float c, bool split, CUtensorMap *tm, Params *p) {
   const uint64_t rowb = kHeadDim * 2;
   if (!encode_3d(&tm[0], q, kHeadDim, T, heads, rowb, rowb * T, kHeadDim, kBlockM) ||
       !encode_3d(&tm[1], k, kHeadDim, T, kv_heads, rowb, rowb * T, kHeadDim, kBlockN) ||
@@ -752,7 +878,7 @@ bool prepare(const void *q, const void *k, const void *vT, void *o, float *lse, 
   p->T = T;
   p->heads = heads;
   p->group = heads / kv_heads;
-  p->row_blocks = (T + kUnitRows - 1) / kUnitRows;
+  p->row_blocks = split ? (T + kBlockM - 1) / kBlockM : (T + kUnitRows - 1) / kUnitRows;
   p->units = heads * p->row_blocks;
   p->c = c;
   p->o = static_cast<__half *>(o);
@@ -770,7 +896,8 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, f
   if ((rc = device_state(&st))) return rc;
   CUtensorMap tm[3];
   Params p;
-  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, tm, &p)) return ATTN_ELAUNCH;
+  const bool split = use_split(T, heads, st->sms);
+  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, split, tm, &p)) return ATTN_ELAUNCH;
   unsigned slot;
   bool stall = false;
   {
@@ -785,9 +912,9 @@ extern "C" int attn_fwd(const void *q, const void *k, const void *vT, void *o, f
   p.sched = st->scratch + kScratchSched + 2 * slot;
   const int grid = p.units < st->sms ? p.units : st->sms;
   if (stall)
-    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+    launch_kernel<true>(split, grid, stream, tm, p);
   else
-    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+    launch_kernel<false>(split, grid, stream, tm, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }
@@ -968,11 +1095,7 @@ int noalloc_state(NoAllocState **out) {
         return ATTN_ELAUNCH;
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (cudaFuncSetAttribute(attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return ATTN_ELAUNCH;
+    if (!set_smem_attributes()) return ATTN_ELAUNCH;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
@@ -1008,7 +1131,8 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, vo
   if ((rc = noalloc_state(&st))) return rc;
   CUtensorMap tm[3];
   Params p;
-  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, tm, &p)) return ATTN_ELAUNCH;
+  const bool split = use_split(T, heads, st->sms);
+  if (!prepare(q, k, vT, o, lse, T, heads, kv_heads, c, split, tm, &p)) return ATTN_ELAUNCH;
   unsigned slot;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -1024,13 +1148,20 @@ extern "C" int attn_fwd_noalloc(const void *q, const void *k, const void *vT, vo
     return ATTN_ELAUNCH;
   }
   const int grid = p.units < st->sms ? p.units : st->sms;
-  attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm[0], tm[1], tm[2], p);
+  launch_kernel<false>(split, grid, stream, tm, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   if (status && cudaMemcpyAsync(status, p.status, sizeof(int), cudaMemcpyDefault, stream) !=
                     cudaSuccess) {
     cudaGetLastError();
     return ATTN_ELAUNCH;
   }
+  return ATTN_OK;
+}
+
+extern "C" int attn_test_set_split_mode(int mode) {
+  if (mode < -1 || mode > 1) return ATTN_EINVAL;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_split_mode = mode;
   return ATTN_OK;
 }
 
