@@ -15,6 +15,7 @@ in it.  Each launch is timed with CUDA events on the launching stream.
   python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
   python bench.py --pass backward ...    # the backward pass instead (see below)
   python bench.py --all-configs          # one line per workload: timing + full parity
+  python bench.py --all-configs --pass backward   # the same for the backward call
 
 The --all-configs mode (one GPU) prints one JSON line per workload of the
 benchmark list: the kernel's time (CUDA events; the three small workloads as
@@ -1106,12 +1107,120 @@ def run_all_configs(args):
         torch.cuda.empty_cache()
 
 
+def run_all_configs_backward(args):
+    """One line per workload for the backward call: its time (CUDA events), TFLOP/s over
+    the five products, and its agreement with the fp64 oracle: every element of the three
+    small workloads, 256 query rows and 128 key rows of the two large ones."""
+    import torch
+
+    import oracle
+    import transformer_causal_gqa_gb300 as tcg
+    from transformer_causal_gqa_gb300 import build as tcg_build
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    tcg_build.build()
+    tcg.load_library()
+    c, s_nat = synthetic.scale_c(), 0.125
+    peak, peak_note = measured_peak()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    host = {"cpu_model": cpu_model(), "hardware_concurrency": os.cpu_count(),
+            "oracle_threads": oracle.max_threads()}
+
+    def agreement(got, ref):
+        got = np.asarray(got, dtype=np.float64)
+        return {"rel_frobenius": float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)),
+                "max_err_over_max_ref": float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))}
+
+    for w in synthetic.WORKLOADS.values():
+        T, H, G = w.T, w.heads, w.kv_heads
+        inputs = synthetic.make_inputs(w)
+        dO_np = synthetic.make_output_grad(w)
+        q, k, vT = (torch.from_numpy(x).to(dev) for x in inputs)
+        dO = torch.from_numpy(dO_np).to(dev)
+        o, lse = tcg.attention(q, k, vT, c)
+        dq = torch.empty((H, T, 64), dtype=torch.float32, device=dev)
+        dk = torch.empty((G, T, 64), dtype=torch.float32, device=dev)
+        dvT = torch.empty((G, 64, T), dtype=torch.float32, device=dev)
+        ws = torch.empty(tcg.attn_bwd_workspace_bytes(T, H, G), dtype=torch.uint8, device=dev)
+
+        def step():
+            tcg.attn_bwd(q, k, vT, o, lse, dO, dq, dk, dvT, T, H, G, c, s_nat, ws, stream)
+
+        step()
+        if tcg.bwd_last_device_status(stream) != tcg.ATTN_OK:
+            raise RuntimeError(f"{w.name}: backward device status is not OK")
+        got = (dq.cpu().numpy(), dk.cpu().numpy(), dvT.cpu().numpy())
+        o_h, l_h = o.cpu().numpy(), lse.cpu().numpy()
+        for _ in range(max(3, args.warmup)):
+            step()
+        small = T <= 2048
+        per_pair = 50 if small else 1
+        pairs = 20 if small else 50
+        sampler = ClockSampler(gpu_uuid())
+        sampler.start()
+        times = []
+        torch.cuda.synchronize()
+        for _ in range(pairs):
+            if not small:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(per_pair):
+                step()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        if tcg.bwd_last_device_status(stream) != tcg.ATTN_OK:
+            raise RuntimeError(f"{w.name}: backward device status after timing is not OK")
+        ms = [a.elapsed_time(b) / per_pair for a, b in times]
+        t0 = time.perf_counter()
+        if small:
+            rq, rk, rv, _ = oracle.attn_bwd(*inputs, o_h, l_h, dO_np, T, H, G, c, s_nat)
+            rows = "every element"
+            parity = {"dQ": agreement(got[0], rq), "dK": agreement(got[1], rk),
+                      "dV^T": agreement(got[2], rv)}
+        else:
+            rng = np.random.default_rng(w.seed)
+            qh, qi = rng.integers(0, H, 256), rng.integers(0, T, 256)
+            kg, kj = rng.integers(0, G, 128), rng.integers(0, T, 128)
+            rq, rk, rv = oracle.attn_bwd_rows(*inputs, o_h, l_h, dO_np, T, H, G, c, s_nat,
+                                              qh, qi, kg, kj)
+            rows = "256 query rows (dQ) and 128 key rows (dK, dV) drawn uniformly"
+            parity = {"dQ": agreement(got[0][qh, qi], rq), "dK": agreement(got[1][kg, kj], rk),
+                      "dV^T": agreement(got[2][kg, :, kj], rv)}
+        oracle_s = time.perf_counter() - t0
+        med = statistics.median(ms)
+        flops = bwd_flops(w)
+        tflops = flops / (med / 1e3) / 1e12
+        print(json.dumps({
+            "mode": "all-configs", "pass": "backward", "workload": w.name, "T": T, "heads": H,
+            "kv_heads": G, "gpu_ms_median": med, "gpu_ms_mean": statistics.fmean(ms),
+            "gpu_ms_min": min(ms), "event_pairs": pairs, "launches_per_event_pair": per_pair,
+            "l2": ("warm: back-to-back calls inside each event pair" if small else
+                   "flushed before each call (512 MiB write)"),
+            "flops_five_products": flops, "tflops": tflops, "frac_of_measured_peak": tflops / peak,
+            "peak": peak, "peak_source": peak_note,
+            "frac_of_datasheet_fp16": tflops / DATASHEET_FP16_TFLOPS,
+            "oracle_rows": rows, "parity": parity, "oracle_s": oracle_s, **host, "clocks": clocks,
+        }), flush=True)
+        del q, k, vT, dO, o, lse, dq, dk, dvT, ws, got
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
     if args.all_configs:
         if args.impl == "reference":
             raise SystemExit("--all-configs times the GPU kernel; the oracle is timed inside it")
-        run_all_configs(args)
+        if args.which == "backward":
+            run_all_configs_backward(args)
+        elif args.which == "forward":
+            run_all_configs(args)
+        else:
+            raise SystemExit("--all-configs covers --pass forward and --pass backward")
         return
     if args.which == "producer":
         (run_reference_producer if args.impl == "reference" else run_gb300_producer)(args)
