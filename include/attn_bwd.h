@@ -32,14 +32,24 @@
  *   dvT  binary32 [kv_heads][64][T]              -- output
  *
  * Ownership: the caller owns every buffer, including `workspace`, where the
- * call keeps the row terms D (binary32 [heads][T]) between its two launches.
- * The library allocates a 4-byte status word per device on first use and
- * never frees it; nothing is allocated per call.
+ * call keeps the row terms D (binary32 [heads][T]) between its launches and,
+ * for short problems, partial dK and dV^T planes (below).  The library
+ * allocates a 4-byte status word per device on first use and never frees it;
+ * nothing is allocated per call.
+ *
+ * Short problems: the key launch has one unit per (K/V head, 128-key tile),
+ * each walking every query head of its group over every later query tile.
+ * When that gives fewer than 128 units, a group of two or more heads and a
+ * longest walk of at least 16 steps (group * ceil(T / 128)), each pair's steps
+ * are shared out over S = min(group, ceil(256 / units), 8) units that write
+ * partial sums into the workspace, and a third launch adds the S planes in a
+ * fixed order (so results stay deterministic, and differ from the unsplit sum
+ * only by the order of the binary32 additions).  S depends on the shape only.
  *
  * Errors: every entry point returns an attn_status (attn_fwd.h).  Argument
- * errors are detected on the host before anything is launched.  The two
- * launches (the query kernel, then the key kernel) are asynchronous and
- * ordered on `stream`.
+ * errors are detected on the host before anything is launched.  The launches
+ * (the query kernel, the key kernel, and for short problems the sum of the
+ * partial planes) are asynchronous and ordered on `stream`.
  */
 #ifndef ATTN_BWD_H
 #define ATTN_BWD_H
@@ -54,8 +64,10 @@ extern "C" {
 
 /*
  * attn_bwd_workspace_bytes -- device bytes attn_bwd needs as `workspace` for
- * the given shape (heads * T * 4, rounded up to 256 bytes), or 0 if the
- * shape is not admitted.
+ * the given shape, or 0 if the shape is not admitted: heads * T * 4 rounded up
+ * to 256 bytes, plus, for the short problems whose key launch is split (above),
+ * two arrays of S partial planes of kv_heads * T * 64 binary32 values, each
+ * rounded up to 256 bytes.
  */
 size_t attn_bwd_workspace_bytes(int T, int heads, int kv_heads);
 

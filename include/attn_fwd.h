@@ -153,8 +153,9 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *vT, void *o, floa
  * attn_test_inject_stall -- test hook for the kernel's failure detection.
  *
  * The source pages have no counterpart of this entry point.  It makes the
- * next attn_fwd launch in this process skip the first K-tile copy of its
- * first CTA.  The wait on the missing tile then runs out after 1 s: the CTA
+ * next attn_fwd launch in this process skip the Q-tile copy of its work unit
+ * 0 (the heaviest, whichever CTA takes it).  The wait on the missing tile
+ * then runs out after 1 s: the CTA
  * records a timeout, drains the copies and MMAs it issued, frees its tensor
  * memory and exits; attn_last_device_status then returns ATTN_ETIMEOUT (and
  * clears the status word and the scheduler's counters), and later launches

@@ -148,8 +148,18 @@ def test_bwd_rejects_overlaps(lib):
 
 
 def test_bwd_workspace_bytes(lib):
+    # 512 key-launch units (8 K/V heads x 64 tiles): the row terms only
     assert tcg.attn_bwd_workspace_bytes(8192, 32, 8) == 32 * 8192 * 4
-    assert tcg.attn_bwd_workspace_bytes(64, 3, 1) == 768        # T % 64 == 0: already 256-aligned
+    assert tcg.attn_bwd_workspace_bytes(16384, 4, 1) == 4 * 16384 * 4     # 128 units
+    # short GQA problems add S partial planes of dK and of dV^T,
+    # S = min(group, ceil(256 / units), 8): 4 K/V heads x 16 tiles, groups of 4 -> S = 4
+    up = lambda n: (n + 255) // 256 * 256
+    plane = 4 * 2048 * 64 * 4
+    assert tcg.attn_bwd_workspace_bytes(2048, 16, 4) == up(16 * 2048 * 4) + 2 * up(4 * plane)
+    plane = 2 * 1024 * 64 * 4                                          # 2 K/V heads x 8 tiles, groups of 8
+    assert tcg.attn_bwd_workspace_bytes(1024, 16, 2) == up(16 * 1024 * 4) + 2 * up(8 * plane)
+    assert tcg.attn_bwd_workspace_bytes(1024, 12, 12) == 12 * 1024 * 4  # MHA: no split
+    assert tcg.attn_bwd_workspace_bytes(64, 3, 1) == 768        # a 3-step walk: no split
     assert tcg.attn_bwd_workspace_bytes(100, 4, 2) == 0
 
 

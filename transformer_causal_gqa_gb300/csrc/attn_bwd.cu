@@ -145,6 +145,13 @@ struct BwdParams {
   float *dq;          // [H][T][64]
   float *dk;          // [G][T][64]
   float *dvT;         // [G][64][T]
+  // Short problems: each key-launch unit's steps are shared out over `splits`
+  // units, each writing its partial dK (already times s) and dV^T into plane
+  // `split` of these workspace arrays, [splits][G][T][64] and [splits][G][64][T];
+  // a reduce launch sums the planes.  splits == 1: written to dk, dvT directly.
+  int splits;
+  float *dk_part;
+  float *dv_part;
   int *status;
   int stall;          // test hook: CTA 0 of the query launch never loads its first K/V stage
 };
@@ -496,28 +503,39 @@ constexpr int kThreads = 32 * 12;
 constexpr uint32_t kSQ = 0, kSDO = kTileBytes, kSL = 2 * kTileBytes, kSDd = kSL + kTile * 4;
 
 struct Unit {
-  int g, kt, nq, steps;   // query tiles kt .. kt + nq - 1 for each of the group's heads
+  int g, kt, nq;    // query tiles kt .. kt + nq - 1 for each of the group's heads
+  int split;        // which share of the (K/V head, key tile) pair's steps
+  int first, steps; // this unit's steps: first .. first + steps - 1 of the pair's
 };
+__device__ __forceinline__ int key_units(const BwdParams &p) {
+  return p.kv_heads * p.q_tiles * p.splits;
+}
 __device__ __forceinline__ Unit decode(int u, const BwdParams &p) {
   Unit w;
-  const int r = u / p.kv_heads;
-  w.g = u - r * p.kv_heads;
+  const int per_tile = p.kv_heads * p.splits;
+  const int r = u / per_tile;
+  const int rem = u - r * per_tile;
+  w.g = rem / p.splits;
+  w.split = rem - w.g * p.splits;
   w.kt = r;                      // earliest key tiles see the most query tiles
   w.nq = p.q_tiles - w.kt;
-  w.steps = p.group * w.nq;
+  const int total = p.group * w.nq;
+  w.first = (int)((long long)total * w.split / p.splits);
+  w.steps = (int)((long long)total * (w.split + 1) / p.splits) - w.first;
   return w;
 }
 // step i of a unit: query head and query tile
 __device__ __forceinline__ void step_of(const Unit &w, int i, const BwdParams &p, int &h, int &qt) {
-  const int z = i / w.nq;
+  const int j = w.first + i;
+  const int z = j / w.nq;
   h = w.g * p.group + z;
-  qt = w.kt + (i - z * w.nq);
+  qt = w.kt + (j - z * w.nq);
 }
 
 __device__ void load_role(const CUtensorMap *tmK, const CUtensorMap *tmVT, const CUtensorMap *tmQ,
                           const CUtensorMap *tmDO, const BwdParams &p, const Sync &sy,
                           uint32_t smem) {
-  const int units = p.kv_heads * p.q_tiles;
+  const int units = key_units(p);
   uint32_t pos = 0, pos_issued = 0, kv_issued = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
@@ -558,7 +576,7 @@ drain:
 __device__ void sdp_role(const BwdParams &p, const Sync &sy, uint32_t smem, uint32_t tmem) {
   constexpr uint32_t idS = idesc_f16_f32(kTile, kTile);
   constexpr uint32_t idDP = idesc_f16_f32_mn(kTile, kTile, true, false);
-  const int units = p.kv_heads * p.q_tiles;
+  const int units = key_units(p);
   uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
@@ -597,7 +615,7 @@ drain:
 __device__ void acc_role(int which, const BwdParams &p, const Sync &sy, uint32_t smem,
                          uint32_t tmem) {
   constexpr uint32_t id = idesc_f16_f32_mn(kTile, kD, false, true);
-  const int units = p.kv_heads * p.q_tiles;
+  const int units = key_units(p);
   const uint32_t a_col = which ? kColDS : kColP;
   const uint32_t d_col = which ? kColDK : kColDV;
   const uint32_t b_off = which ? kSQ : kSDO;
@@ -683,7 +701,7 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
   const bool leader = (threadIdx.x & 31) == 0;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const float c = p.c;
-  const int units = p.kv_heads * p.q_tiles;
+  const int units = key_units(p);
   uint32_t pos = 0;
   int k = 0;
   for (int u = unit_of(0, units); u >= 0; u = unit_of(++k, units)) {
@@ -726,18 +744,28 @@ __device__ void compute_role(const BwdParams &p, const Sync &sy, const uint8_t *
       __syncwarp();
       if (leader) mbar_arrive(sy.bar(kBarPFull + half));
     }
-    // epilogue: the first half writes dV^T, the second s dK, for this key row
-    if (!sy.wait2_warp(kBarDone, (pos - 1) & 1, 235, kBarDone + 1, (pos - 1) & 1, 236)) return;
-    tc_fence_after();
+    // epilogue: the first half writes dV^T, the second s dK, for this key row (into
+    // the unit's partial planes when the pair's steps are shared out; a share with
+    // no steps writes zeros)
     uint32_t ar[64];
-    tmem_ld_x64(tmem + lane_base + (half ? kColDK : kColDV), ar);
+    if (w.steps > 0) {
+      if (!sy.wait2_warp(kBarDone, (pos - 1) & 1, 235, kBarDone + 1, (pos - 1) & 1, 236)) return;
+      tc_fence_after();
+      tmem_ld_x64(tmem + lane_base + (half ? kColDK : kColDV), ar);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kD; ++e) ar[e] = 0u;
+    }
     if (key < p.T) {
+      const size_t plane = (size_t)p.kv_heads * p.T * kD;
+      float *dv_base = p.splits > 1 ? p.dv_part + plane * w.split : p.dvT;
+      float *dk_base = p.splits > 1 ? p.dk_part + plane * w.split : p.dk;
       if (half == 0) {
-        float *dvt = p.dvT + (size_t)w.g * kD * p.T + key;
+        float *dvt = dv_base + (size_t)w.g * kD * p.T + key;
 #pragma unroll
         for (int e = 0; e < kD; ++e) dvt[(size_t)e * p.T] = __uint_as_float(ar[e]);
       } else {
-        float4 *dk = reinterpret_cast<float4 *>(p.dk + ((size_t)w.g * p.T + key) * kD);
+        float4 *dk = reinterpret_cast<float4 *>(dk_base + ((size_t)w.g * p.T + key) * kD);
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           dk[e] = make_float4(__uint_as_float(ar[4 * e]) * p.s, __uint_as_float(ar[4 * e + 1]) * p.s,
@@ -805,6 +833,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 }  // namespace klaunch
 
+// The sum over the key launch's partial planes (short problems only): out[x] =
+// sum over i of part[i n + x], in order i = 0, 1, ... (deterministic), for dK and
+// dV^T at once.  n is a multiple of 4 (whole 64-wide rows).
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float *dk_part, const float *dv_part,
+                                                            float *dk, float *dvT, size_t n,
+                                                            int splits) {
+  const size_t n4 = n / 4;
+  for (size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x; x < 2 * n4;
+       x += (size_t)gridDim.x * blockDim.x) {
+    const bool second = x >= n4;
+    const size_t y = second ? x - n4 : x;
+    const float4 *src = reinterpret_cast<const float4 *>(second ? dv_part : dk_part) + y;
+    float4 acc = src[0];
+    for (int i = 1; i < splits; ++i) {
+      const float4 v = src[(size_t)i * n4];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4 *>(second ? dvT : dk)[y] = acc;
+  }
+}
+
 // ============================================================================ host side
 struct BwdState {
   bool ready = false;
@@ -865,9 +917,31 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
 
 size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+// Short problems share each (K/V head, key tile) pair's steps out over several
+// key-launch units.  With fewer than 128 units, the key launch's longest unit --
+// a whole group of query heads over every later query tile, group * q_tiles
+// steps -- bounds the call; the query launch's longest is q_tiles steps.  So a
+// group of two or more heads whose chain is at least 16 steps gets
+// S = min(group, ceil(256 / units), 8) shares (at least one step each), and a
+// reduce launch adds them.  A function of the shape alone, so the workspace
+// size is too.
+int key_splits(int T, int heads, int kv_heads) {
+  const int q_tiles = (T + kTile - 1) / kTile;
+  const int group = heads / kv_heads;
+  const long long units = (long long)kv_heads * q_tiles;
+  if (units >= 128 || group < 2 || (long long)group * q_tiles < 16) return 1;
+  long long s = (256 + units - 1) / units;
+  if (s > group) s = group;
+  return (int)(s < 8 ? s : 8);
+}
+
 // Workspace: the row terms D (binary32 [heads][T]) the query launch writes
-// for the key launch.
-size_t bwd_workspace(int T, int heads) { return up256((size_t)heads * T * 4); }
+// for the key launch; with split key units, their partial dK and dV^T planes.
+size_t bwd_workspace(int T, int heads, int kv_heads) {
+  const int sp = key_splits(T, heads, kv_heads);
+  const size_t plane = (size_t)kv_heads * T * kD * 4;
+  return up256((size_t)heads * T * 4) + (sp > 1 ? 2 * up256(plane * sp) : 0);
+}
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -888,7 +962,7 @@ int check_bwd_shape(int T, int heads, int kv_heads, float c, float s) {
 
 extern "C" size_t attn_bwd_workspace_bytes(int T, int heads, int kv_heads) {
   if (check_bwd_shape(T, heads, kv_heads, 1.f, 1.f)) return 0;
-  return bwd_workspace(T, heads);
+  return bwd_workspace(T, heads, kv_heads);
 }
 
 extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void *o,
@@ -908,7 +982,7 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   for (const void *ptr : outs)
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return ATTN_EALIGN;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_EALIGN;
-  const size_t ws_bytes = bwd_workspace(T, heads);
+  const size_t ws_bytes = bwd_workspace(T, heads, kv_heads);
   if (workspace_bytes < ws_bytes) return ATTN_EINVAL;
   const size_t hq = (size_t)heads * T * kD, kvn = (size_t)kv_heads * T * kD;
   const size_t in_sizes[] = {hq * 2, kvn * 2, kvn * 2, hq * 2, (size_t)heads * T * 4, hq * 2};
@@ -948,13 +1022,26 @@ extern "C" int attn_bwd(const void *q, const void *k, const void *vT, const void
   p.dq = dq;
   p.dk = dk;
   p.dvT = dvT;
+  p.splits = key_splits(T, heads, kv_heads);
+  {
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t plane = (size_t)kv_heads * T * kD * 4;
+    p.dk_part = reinterpret_cast<float *>(ws + up256((size_t)heads * T * 4));
+    p.dv_part = reinterpret_cast<float *>(ws + up256((size_t)heads * T * 4) + up256(plane * p.splits));
+  }
   p.status = st->status;
   p.stall = g_bwd_stall.exchange(0);
-  const int qunits = heads * p.q_tiles, kunits = kv_heads * p.q_tiles;
+  const int qunits = heads * p.q_tiles, kunits = kv_heads * p.q_tiles * p.splits;
   qlaunch::query_kernel<<<qunits < st->sms ? qunits : st->sms, qlaunch::kThreads,
                           qlaunch::kSmemBytes, stream>>>(tmQ, tmDO, tmO, tmK, tmVT, p);
   klaunch::key_kernel<<<kunits < st->sms ? kunits : st->sms, klaunch::kThreads,
                         klaunch::kSmemBytes, stream>>>(tmK, tmVT, tmQ, tmDO, p);
+  if (p.splits > 1) {
+    const size_t n = (size_t)kv_heads * T * kD;
+    const size_t blocks = (2 * n / 4 + 255) / 256;
+    reduce_splits_kernel<<<(unsigned)(blocks < 4u * (size_t)st->sms ? blocks : 4u * (size_t)st->sms),
+                           256, 0, stream>>>(p.dk_part, p.dv_part, dk, dvT, n, p.splits);
+  }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }

@@ -292,7 +292,9 @@ __device__ __forceinline__ void mul2(float &d0, float &d1, float b) {
 // TMA warp (one lane): takes units from the global work counter and publishes
 // them to the CTA's unit queue; for each, loads the two Q subtiles into the
 // unit's Q buffer, then K(j), V^T(j) for j = 0 .. n1-1 through the ring.
-// kStallHook (test builds of the launch only): CTA 0 skips its first K tile, so a wait runs out.
+// kStallHook (test builds of the launch only): the Q tile of work unit 0 (whichever CTA
+// claims it) is never loaded.  Both subtiles need it in either mode, so their S issue
+// waits until it runs out.
 template <bool kStallHook, bool kSplit>
 __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                           const Params &p, const Sync &sy, uint32_t smem) {
@@ -312,10 +314,13 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
     if (!sy.wait(kBarQEmpty + qb, ((k >> 1) & 1) ^ 1, 1)) goto drain;
     ++q_issued;
     const uint32_t qdst = smem + kOffQ + qb * 2 * kTileBytes;
-    // split mode: one Q tile, read by both subtiles
-    mbar_arrive_expect_tx(sy.bar(kBarQFull + qb), (kSplit ? 1 : 2) * kTileBytes);
-    tma_load_3d(qdst, tmQ, sy.bar(kBarQFull + qb), 0, w.row0, w.h);
-    if (!kSplit) tma_load_3d(qdst + kTileBytes, tmQ, sy.bar(kBarQFull + qb), 0, w.row0 + kBlockM, w.h);
+    if (!(kStallHook && u == 0)) {  // test hook: this Q tile never arrives
+      // split mode: one Q tile, read by both subtiles
+      mbar_arrive_expect_tx(sy.bar(kBarQFull + qb), (kSplit ? 1 : 2) * kTileBytes);
+      tma_load_3d(qdst, tmQ, sy.bar(kBarQFull + qb), 0, w.row0, w.h);
+      if (!kSplit)
+        tma_load_3d(qdst + kTileBytes, tmQ, sy.bar(kBarQFull + qb), 0, w.row0 + kBlockM, w.h);
+    }
     for (int jp = 0; jp < (kSplit ? w.ring / 2 : w.n1); ++jp) {
       // the key tile of pair jp
       int j = jp;
@@ -326,8 +331,6 @@ __device__ void load_role(const CUtensorMap *tmQ, const CUtensorMap *tmK, const 
         const uint32_t dst = smem + kOffRing + rs * kTileBytes;
         const uint32_t full = sy.bar(kBarKvFull + rs);
         pos_issued = pos + 1;
-        if (kStallHook && blockIdx.x == 0 && k == 0 && jp == 0 && kv == 0)
-          continue;  // test hook: this K tile never arrives
         mbar_arrive_expect_tx(full, kTileBytes);
         if (kv == 0) {
           tma_load_3d(dst, tmK, full, 0, j * kBlockN, w.g);
