@@ -84,6 +84,8 @@ BWD_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_bw
 BWD_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_bwd_t8192_h32_kv8.md")
 QKV_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_qkv.cu")
 QKV_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qkv_kernel_t8192_w2048_h32_kv8.md")
+MAT_SOURCE = os.path.join(ROOT, "transformer_causal_gqa_gb300", "csrc", "attn_materialised.cu")
+MAT_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_materialised_t8192_and_t2048.md")
 
 
 def parse_args():
@@ -798,7 +800,13 @@ def run_gb300_materialised(args):
                            workspace_bytes=ws.numel(),
                            parallelism=f"independent problem per GPU x{world}"),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_note,
+                         "frac": achieved / peak,
+                         # counted on 4 query heads over 1 K/V head at T = 8192 and scaled
+                         # by the head count (independent per-head planes, each beyond L2)
+                         "traffic": (kernel_traffic(MAT_TRAFFIC_SUMMARY, MAT_SOURCE,
+                                                    "traffic_bytes_per_call")
+                                     if args.workload == synthetic.HEADLINE else None),
+                         "peak_source": peak_note,
                          "kernel": "attn_fwd_materialised call (scores, softmax, pv kernels)",
                          "launch_ms": {"mean": avg_s * 1e3,
                                        "median": statistics.median(per_call_ms),
