@@ -111,11 +111,19 @@ def status_string(status: int) -> str:
 def _stream_handle(stream):
     if stream is None:
         import torch
+        # torch's current stream as a raw handle, without building a Stream object
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return ctypes.c_void_p(raw(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
 
 
 def _check_tensor(name, t, dtype, shape, device=True):
+    # one combined test for the usual case; the separate tests below name the failure
+    if (t.dtype is dtype and t.shape == shape and t.is_contiguous()
+            and (t.is_cuda if device else t.device.type == "cpu")):
+        return
     import torch
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
