@@ -177,6 +177,38 @@ def test_rejections_on_device():
     assert tcg.last_device_status() == tcg.ATTN_OK
 
 
+def test_binding_rejects_bad_cuda_tensors():
+    """The binding's checks on CUDA tensors: each bad argument raises its own error
+    before the library is called, so the output is left as it was."""
+    dev = torch.device("cuda:0")
+    T, H, G = 128, 4, 2
+    q = torch.zeros(H, T, 64, dtype=torch.float16, device=dev)
+    k = torch.zeros(G, T, 64, dtype=torch.float16, device=dev)
+    vT = torch.zeros(G, 64, T, dtype=torch.float16, device=dev)
+    lse = torch.zeros(H, T, dtype=torch.float32, device=dev)
+    sentinel = torch.full((T, H * 64), 7.0, dtype=torch.float16, device=dev)
+    o = sentinel.clone()
+    cases = [
+        ((q.float(), k, vT, o, lse), TypeError),                                # dtype
+        ((q, k[:, :64], vT, o, lse), ValueError),                               # shape
+        ((q, k, vT.clone(), o, lse), None),                                     # valid: accepted
+        ((q, k, torch.zeros(G, T, 64, dtype=torch.float16, device=dev).transpose(1, 2), o, lse),
+         ValueError),                                                           # not contiguous
+        ((q, k, vT, o, lse.cpu()), ValueError),                                 # not on the device
+    ]
+    for args, err in cases:
+        if err is None:
+            tcg.attn_fwd(*args, T, H, G, 0.18)
+            torch.cuda.synchronize()
+            o.copy_(sentinel)
+            continue
+        with pytest.raises(err):
+            tcg.attn_fwd(*args, T, H, G, 0.18)
+        torch.cuda.synchronize()
+        assert torch.equal(o, sentinel)
+    assert tcg.last_device_status() == tcg.ATTN_OK
+
+
 def compare_arrays(q, k, vT, T, H, G):
     c = synthetic.scale_c()
     o, lse = run_gpu(q, k, vT, T, H, G, c)
