@@ -78,6 +78,21 @@ int attn_fwd_materialised(const void *q, const void *k, const void *vT, void *o,
  */
 int attn_materialised_last_device_status(cudaStream_t stream);
 
+/*
+ * attn_materialised_test_inject_stall -- test hook for the materialised
+ * path's failure detection.
+ *
+ * The source pages have no counterpart of this entry point.  It makes the
+ * next attn_fwd_materialised call's scores launch skip the K-tile copy of its
+ * first block.  That block's wait runs out after 1 s: it records a timeout,
+ * stores nothing, waits (bounded) for its other copy, frees its tensor memory
+ * and exits; the other blocks and the two later launches run as usual (on a
+ * scores tile that was not written, so that call's outputs are not valid);
+ * attn_materialised_last_device_status then returns ATTN_ETIMEOUT, and later
+ * calls run normally.  Always returns ATTN_OK.
+ */
+int attn_materialised_test_inject_stall(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,6 +71,19 @@ int attn_qkv_rope(const void *x, const void *w, const float *cosines, const floa
  */
 int attn_qkv_last_device_status(cudaStream_t stream);
 
+/*
+ * attn_qkv_test_inject_stall -- test hook for the producer's failure detection.
+ *
+ * The source pages have no counterpart of this entry point.  It makes the
+ * next attn_qkv_rope call's first CTA skip the X half of its first shared-
+ * memory stage.  The MMA warp's wait on that stage runs out after 1 s: the CTA
+ * records a timeout, lets the copies it issued land, frees its tensor memory
+ * and exits; the other CTAs run as usual (so that call's outputs are not
+ * valid); attn_qkv_last_device_status then returns ATTN_ETIMEOUT, and later
+ * calls run normally.  Always returns ATTN_OK.
+ */
+int attn_qkv_test_inject_stall(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,4 +1,4 @@
-"""Failure detection on the GPU without a fault: a wait inside the kernel runs
+"""Failure detection on the GPU without a fault, for every entry point: a wait inside a kernel runs
 out (its tile is never loaded), the kernel reports ATTN_ETIMEOUT through the
 status word and exits cleanly, and the next launch is correct."""
 import time
@@ -72,3 +72,60 @@ def test_backward_wait_runs_out_then_recovers():
     assert tcg.bwd_last_device_status() == tcg.ATTN_OK
     for a, b in zip(good, again):
         assert torch.equal(a, b)
+
+
+def test_producer_wait_runs_out_then_recovers():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tcg_build.build()
+    lib = tcg.load_library()
+    T, width, H, G = 512, 256, 8, 2
+    dev = torch.device("cuda:0")
+    x, wt, cs, sn = (torch.from_numpy(a).to(dev)
+                     for a in synthetic.make_producer_inputs(T, width, H, G, seed=33))
+    good = [t.cpu() for t in tcg.qkv_rope(x, wt, cs, sn, H, G)]
+    assert tcg.qkv_last_device_status() == tcg.ATTN_OK
+
+    assert lib.attn_qkv_test_inject_stall() == tcg.ATTN_OK
+    t0 = time.monotonic()
+    tcg.qkv_rope(x, wt, cs, sn, H, G)
+    assert tcg.qkv_last_device_status() == tcg.ATTN_ETIMEOUT
+    assert time.monotonic() - t0 < 10.0
+    assert tcg.qkv_last_device_status() == tcg.ATTN_OK    # reading it cleared it
+
+    # the context is usable and the next call reproduces the good result bit for bit
+    again = [t.cpu() for t in tcg.qkv_rope(x, wt, cs, sn, H, G)]
+    assert tcg.qkv_last_device_status() == tcg.ATTN_OK
+    for a, b in zip(good, again):
+        assert torch.equal(a, b)
+
+
+def test_materialised_wait_runs_out_then_recovers():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tcg_build.build()
+    lib = tcg.load_library()
+    w = synthetic.custom(512, 4, 2, seed=34)
+    q, k, vT = synthetic.make_inputs(w)
+    c = synthetic.scale_c()
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (torch.from_numpy(a).to(dev) for a in (q, k, vT))
+    o = torch.empty((w.T, w.heads * 64), dtype=torch.float16, device=dev)
+    lse = torch.empty((w.heads, w.T), dtype=torch.float32, device=dev)
+    ws = torch.empty(tcg.attn_materialised_workspace_bytes(w.T, w.heads, w.kv_heads),
+                     dtype=torch.uint8, device=dev)
+    tcg.attn_fwd_materialised(qd, kd, vd, o, lse, w.T, w.heads, w.kv_heads, c, ws)
+    good = (o.cpu(), lse.cpu())
+    assert tcg.materialised_last_device_status() == tcg.ATTN_OK
+
+    assert lib.attn_materialised_test_inject_stall() == tcg.ATTN_OK
+    t0 = time.monotonic()
+    tcg.attn_fwd_materialised(qd, kd, vd, o, lse, w.T, w.heads, w.kv_heads, c, ws)
+    assert tcg.materialised_last_device_status() == tcg.ATTN_ETIMEOUT
+    assert time.monotonic() - t0 < 10.0
+    assert tcg.materialised_last_device_status() == tcg.ATTN_OK    # reading it cleared it
+
+    # the context is usable and the next call reproduces the good result bit for bit
+    tcg.attn_fwd_materialised(qd, kd, vd, o, lse, w.T, w.heads, w.kv_heads, c, ws)
+    assert tcg.materialised_last_device_status() == tcg.ATTN_OK
+    assert torch.equal(o.cpu(), good[0]) and torch.equal(lse.cpu(), good[1])

@@ -40,7 +40,8 @@ EXPORTED = ("attn_fwd", "attn_fwd_workspace_bytes", "attn_fwd_host",
             "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
             "attn_bwd_last_device_status", "attn_bwd_test_inject_stall", "attn_fwd_materialised",
             "attn_materialised_workspace_bytes", "attn_materialised_last_device_status",
-            "attn_qkv_rope", "attn_qkv_last_device_status")
+            "attn_materialised_test_inject_stall",
+            "attn_qkv_rope", "attn_qkv_last_device_status", "attn_qkv_test_inject_stall")
 
 _lib = None
 
@@ -96,10 +97,14 @@ def load_library():
     lib.attn_materialised_workspace_bytes.restype = sz
     lib.attn_materialised_last_device_status.argtypes = [vp]
     lib.attn_materialised_last_device_status.restype = i
+    lib.attn_materialised_test_inject_stall.argtypes = []
+    lib.attn_materialised_test_inject_stall.restype = i
     lib.attn_qkv_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
     lib.attn_qkv_rope.restype = i
     lib.attn_qkv_last_device_status.argtypes = [vp]
     lib.attn_qkv_last_device_status.restype = i
+    lib.attn_qkv_test_inject_stall.argtypes = []
+    lib.attn_qkv_test_inject_stall.restype = i
     _lib = lib
     return lib
 

@@ -23,6 +23,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "attn_materialised.h"
@@ -46,6 +47,7 @@ struct MatParams {
   __half *o;       // [T][H*64]
   float *lse;      // [H][T]
   int *status;
+  int stall;       // test hook: the scores kernel's first block never loads its K tile
 };
 
 // Bounded wait on an mbarrier phase; records `where` in the status word on expiry.
@@ -106,7 +108,8 @@ __global__ void __launch_bounds__(128) scores_kernel(const __grid_constant__ CUt
     mbar_fence_init();
     mbar_arrive_expect_tx(bar_full, 2 * kTileBytes);
     tma_load_3d(smem, &tmQ, bar_full, 0, qt * kTile, h);
-    tma_load_3d(smem + kTileBytes, &tmK, bar_full, 0, kt * kTile, g);
+    if (!(p.stall && blockIdx.x == 0 && blockIdx.y == 0))   // test hook: this K tile never lands
+      tma_load_3d(smem + kTileBytes, &tmK, bar_full, 0, kt * kTile, g);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), 128);
@@ -377,6 +380,7 @@ struct MatState {
 };
 std::mutex g_mat_mutex;
 MatState g_mat[64];
+std::atomic<int> g_mat_stall{0};   // test hook: the next attn_fwd_materialised call stalls one block
 PFN_cuTensorMapEncodeTiled_v12000 g_mat_encode = nullptr;
 
 int mat_state(MatState **out) {
@@ -495,6 +499,7 @@ extern "C" int attn_fwd_materialised(const void *q, const void *k, const void *v
   p.o = static_cast<__half *>(o);
   p.lse = lse;
   p.status = st->status;
+  p.stall = g_mat_stall.exchange(0);
 
   const uint64_t rowb = kD * 2, trow = (uint64_t)T * 2;
   CUtensorMap tmQ, tmK, tmP, tmVT, tmS;
@@ -524,4 +529,9 @@ extern "C" int attn_materialised_last_device_status(cudaStream_t stream) {
     return ATTN_ELAUNCH;
   if (word != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
   return word ? ATTN_ETIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_materialised_test_inject_stall(void) {
+  g_mat_stall.store(1);
+  return ATTN_OK;
 }

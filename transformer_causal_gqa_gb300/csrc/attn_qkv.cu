@@ -25,6 +25,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "attn_qkv.h"
@@ -59,6 +60,7 @@ struct QkvParams {
   const float *cosines, *sines;
   __half *q, *k, *vT;
   int *status;
+  int stall;          // test hook: CTA 0 never loads the X half of its first stage
 };
 
 struct Sync {
@@ -111,7 +113,8 @@ __device__ void load_role(const CUtensorMap *tmX, const CUtensorMap *tmW, const 
       const uint32_t dst = smem + s * kStageBytes;
       mbar_arrive_expect_tx(sy.bar(kBarFull + s), kStageBytes);
       issued = it + 1;
-      tma_load_3d(dst, tmX, sy.bar(kBarFull + s), kc * kBK, m * kBM, 0);
+      if (!(p.stall && blockIdx.x == 0 && it == 0))   // test hook: this X slice never lands
+        tma_load_3d(dst, tmX, sy.bar(kBarFull + s), kc * kBK, m * kBM, 0);
       tma_load_3d(dst + kABytes, tmW, sy.bar(kBarFull + s), kc * kBK, n * kBN, 0);
     }
   }
@@ -268,6 +271,7 @@ struct QkvState {
 };
 std::mutex g_qkv_mutex;
 QkvState g_qkv[64];
+std::atomic<int> g_qkv_stall{0};   // test hook: the next attn_qkv_rope call stalls one CTA
 PFN_cuTensorMapEncodeTiled_v12000 g_qkv_encode = nullptr;
 
 int qkv_state(QkvState **out) {
@@ -372,6 +376,7 @@ extern "C" int attn_qkv_rope(const void *x, const void *w, const float *cosines,
   p.k = static_cast<__half *>(k);
   p.vT = static_cast<__half *>(vT);
   p.status = st->status;
+  p.stall = g_qkv_stall.exchange(0);
   const int pairs = (p.m_tiles + 1) / 2 * p.n_tiles;
   // an even grid: CTAs 2i and 2i + 1 take the two token tiles of a pair
   const int slots = st->sms / 2;
@@ -391,4 +396,9 @@ extern "C" int attn_qkv_last_device_status(cudaStream_t stream) {
     return ATTN_ELAUNCH;
   if (word != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return ATTN_ELAUNCH;
   return word ? ATTN_ETIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_qkv_test_inject_stall(void) {
+  g_qkv_stall.store(1);
+  return ATTN_OK;
 }
