@@ -155,9 +155,10 @@ def test_workload_every_element(name):
     compare_full(synthetic.WORKLOADS[name])
 
 
-# ragged tails (T mod 128 = 64), one tile, several; groups 1, 2, 4, 8
+# ragged tails (T mod 128 = 64), one tile, several; groups 1, 2, 4, 8, and odd ones
+# (6 over 3; 5 over 1, whose short problems share each key unit's steps five ways)
 @pytest.mark.parametrize("T", [64, 128, 192, 320, 1088])
-@pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1)])
+@pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1), (6, 3), (5, 1)])
 def test_shapes_every_element(T, H, G):
     compare_full(synthetic.custom(T, H, G, seed=T * 100 + H * 10 + G + 7))
 

@@ -73,7 +73,7 @@ def test_workload_every_element(name):
 # unit's key tiles and merge; the normal mode gives each subtile its own 128 rows)
 @pytest.mark.parametrize("mode", [0, 1], indirect=True)
 @pytest.mark.parametrize("T", [64, 192, 320, 384, 448, 640, 1088])
-@pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1)])
+@pytest.mark.parametrize("H,G", [(1, 1), (4, 2), (8, 2), (8, 1), (6, 3), (5, 1)])
 def test_shapes_every_element(mode, T, H, G):
     compare_full(synthetic.custom(T, H, G, seed=T * 100 + H * 10 + G))
 
